@@ -1,0 +1,72 @@
+"""Builds libmsa.so in-tree with nvcc for sm_103a (GB300).
+
+Each CUDA source compiles to its own object in parallel under ``_build/``;
+objects newer than every source and header are reused.  The CUDA runtime is
+linked statically and the driver entry point for tensor maps is resolved at run
+time, so the library loads on machines without a GPU driver (its entry points
+then fail with MSA_ERR_CUDA).
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(PKG, "libmsa.so")
+INCLUDE = os.path.join(ROOT, "include")
+
+SOURCES = ["msa_api.cu", "k_regroup.cu", "k_select.cu", "k_fwd.cu", "k_bwd.cu", "k_reduce.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
+         "--expt-relaxed-constexpr", "-I", INCLUDE]
+
+
+def nvcc() -> str:
+    path = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(path):
+        raise RuntimeError("nvcc not found: the CUDA 13 toolkit is required to build libmsa")
+    return path
+
+
+def _deps() -> float:
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "msa.h")]
+    return max(os.path.getmtime(f) for f in files)
+
+
+def _compile(src: str, newest: float, extra: list[str]) -> str:
+    obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+    if os.path.exists(obj) and os.path.getmtime(obj) >= newest:
+        return obj
+    cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+    return obj
+
+
+def build(verbose: bool = False, extra_flags: list[str] | None = None) -> str:
+    """Compile (if needed) and return the path of libmsa.so."""
+    os.makedirs(BUILD, exist_ok=True)
+    newest = _deps()
+    extra = list(extra_flags or [])
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(lambda s: _compile(s, newest, extra), SOURCES))
+    if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
+        tmp = LIB + ".tmp"
+        cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, LIB)
+    if verbose:
+        print("built", LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    build(verbose=True)

@@ -1,0 +1,411 @@
+// Proxy scoring with on-chip 128-key block max-pool and streaming top-k.
+//
+// The proxy head scores every causal key; KV is then chosen in 128-token
+// blocks by the maximum proxy score inside each block ("Dramatically Speeding
+// Up Million-Token Training! ... 'Flash-MSA' ...", ai-minor.com, "What's
+// Happening? News Overview"), each query keeping its top-k blocks with its own
+// diagonal block always included.
+//
+// One CTA per (query block J of a document, KV group g).  For every key block
+// n = 0..J the tensor cores compute the 128x128 score tile q_p . k_p^T into
+// TMEM (K = dp), and the epilogue threads (one TMEM lane = one query row)
+// reduce it to the block maximum and, when the block enters the row's top
+// list, its lowest-index argmax.  Neither the score tile nor the pooled
+// [T, blocks] matrix ever leaves the SM.
+//
+// Roles (320 threads): warps 0-3 and 4-7 are two epilogue warpgroups that take
+// key blocks alternately in pairs (TMEM accumulators 0,1 and 2,3), warp 8
+// issues TMA loads of k_p blocks into a ring, warp 9 issues tcgen05.mma.
+#include <cfloat>
+
+#include "msa_internal.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kSelStages = 6;
+constexpr int kSelThreads = 320;
+constexpr float kTieBand = 1e-3f;
+
+template <int DP>
+struct SelCfg {
+  static constexpr int kRowBytes = DP * 2;
+  static constexpr int kTileBytes = 128 * kRowBytes;
+  static constexpr uint32_t kLayout = DP == 64 ? kLayoutSW128 : kLayoutSW64;
+  static constexpr uint32_t kSBO = 8 * kRowBytes;
+  static constexpr int kSwizzleBytes = DP == 64 ? 128 : 64;
+};
+
+// a ranks ahead of b: higher score, ties to the lower block id (id = block << 8 | arg)
+__device__ __forceinline__ bool better(float sa, uint32_t ia, float sb, uint32_t ib) {
+  return sa > sb || (sa == sb && (ia >> 8) < (ib >> 8));
+}
+
+// Insert (s, nid) into the descending list sc/id (CAP entries), dropping the last.
+template <int CAP>
+__device__ __forceinline__ void list_insert(float (&sc)[CAP], uint32_t (&id)[CAP], float s,
+                                            uint32_t nid) {
+  bool shift = false;
+  float cs = s;
+  uint32_t ci = nid;
+#pragma unroll
+  for (int i = 0; i < CAP; ++i) {
+    const bool take = shift || better(s, nid, sc[i], id[i]);
+    const float ts = sc[i];
+    const uint32_t ti = id[i];
+    sc[i] = take ? cs : ts;
+    id[i] = take ? ci : ti;
+    cs = take ? ts : cs;
+    ci = take ? ti : ci;
+    shift = take;
+  }
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) { return fmaxf(fmaxf(a, b), c); }
+
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+  float m[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) m[i] = max3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  m[10] = fmaxf(v[30], v[31]);
+  return fmaxf(fmaxf(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5])),
+               fmaxf(max3(m[6], m[7], m[8]), fmaxf(m[9], m[10])));
+}
+
+struct SelArgs {
+  const int32_t* cu;
+  const int32_t* cu_blocks;
+  int ndoc, T, hkv, K, nb_bound;
+  float proxy_scale;
+  int32_t* sel_idx;
+  float* sel_score;
+  uint8_t* sel_arg;
+  float* plse;
+  uint8_t* tie;
+  unsigned* status;
+};
+
+template <int DP, int CAP>
+__global__ void __launch_bounds__(kSelThreads, 1)
+    k_select(const __grid_constant__ CUtensorMap tm_qp, const __grid_constant__ CUtensorMap tm_kp,
+             const SelArgs a) {
+  using C = SelCfg<DP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  // ---- shared memory carve-up ----
+  uint8_t* sQ = smem;                                   // q_p tile, 128 rows
+  uint8_t* sK = sQ + C::kTileBytes;                     // k_p ring
+  float* m_sc = reinterpret_cast<float*>(sK + kSelStages * C::kTileBytes);  // [CAP][128]
+  uint32_t* m_id = reinterpret_cast<uint32_t*>(m_sc + CAP * 128);           // [CAP][128]
+  float* d_sc = reinterpret_cast<float*>(m_id + CAP * 128);                 // [128]
+  uint32_t* d_id = reinterpret_cast<uint32_t*>(d_sc + 128);                 // [128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(d_id + 128);
+  // bars: 0 qfull | 1..S kvfull | S+1..2S kvempty | 2S+1..2S+4 accfull | 2S+5..2S+8 accempty
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kSelStages + 9);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  const uint32_t b_qfull = smem_u32(bars);
+  auto b_kvfull = [&](int s) { return smem_u32(bars + 1 + s); };
+  auto b_kvempty = [&](int s) { return smem_u32(bars + 1 + kSelStages + s); };
+  auto b_accfull = [&](int i) { return smem_u32(bars + 1 + 2 * kSelStages + i); };
+  auto b_accempty = [&](int i) { return smem_u32(bars + 5 + 2 * kSelStages + i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item: query block J of document d, group g (heaviest first) ----
+  if (!a.cu_blocks[a.ndoc + 1]) return;  // malformed cu_seqlens (flagged by k_meta)
+  const int nbt = min(a.cu_blocks[a.ndoc], a.nb_bound);
+  const int g = blockIdx.x % a.hkv;
+  const int gb = nbt - 1 - (int)(blockIdx.x / a.hkv);
+  if (gb < 0) return;
+  const int d = doc_of_block(a.cu_blocks, a.ndoc, gb);
+  const int J = gb - a.cu_blocks[d];
+  const int dstart = a.cu[d];
+  const int L = a.cu[d + 1] - dstart;
+  const int qstart = dstart + J * kBlock;
+  const int nrows = min(kBlock, L - J * kBlock);
+  const int nblk = J + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_qfull, 1);
+    for (int s = 0; s < kSelStages; ++s) {
+      mbar_init(b_kvfull(s), 1);
+      mbar_init(b_kvempty(s), 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(b_accfull(i), 1);
+      mbar_init(b_accempty(i), 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tslot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(tslot);
+
+  if (warp == 8) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_qp);
+      tma_prefetch_desc(&tm_kp);
+      mbar_arrive_expect_tx(b_qfull, C::kTileBytes);
+      tma_load_3d(smem_u32(sQ), &tm_qp, b_qfull, 0, g, qstart);
+      for (int n = 0; n < nblk; ++n) {
+        const int s = n % kSelStages;
+        if (n >= kSelStages &&
+            !wait_bar(b_kvempty(s), ((n / kSelStages) & 1) ^ 1, abort_flag, a.status,
+                      wait_site(kKerSelect, 7 + s, n)))
+          break;
+        mbar_arrive_expect_tx(b_kvfull(s), C::kTileBytes);
+        tma_load_3d(smem_u32(sK + s * C::kTileBytes), &tm_kp, b_kvfull(s), 0, g,
+                    dstart + n * kBlock);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------ MMA issuer ---------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16(128, 128, false, false);
+      if (wait_bar(b_qfull, 0, abort_flag, a.status, wait_site(kKerSelect, 0, 0))) {
+        const uint32_t q0 = smem_u32(sQ);
+        for (int n = 0; n < nblk; ++n) {
+          const int s = n % kSelStages, acc = n & 3;
+          if (!wait_bar(b_kvfull(s), (n / kSelStages) & 1, abort_flag, a.status,
+                        wait_site(kKerSelect, 1 + s, n)))
+            break;
+          if (n >= 4 && !wait_bar(b_accempty(acc), ((n >> 2) & 1) ^ 1, abort_flag, a.status,
+                                  wait_site(kKerSelect, 17 + acc, n)))
+            break;
+          tc_fence_after();
+          const uint32_t k0 = smem_u32(sK + s * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const uint64_t ad = make_sdesc(q0 + kk * 32, 16, C::kSBO, C::kLayout);
+            const uint64_t bd = make_sdesc(k0 + kk * 32, 16, C::kSBO, C::kLayout);
+            umma_bf16(tbase + acc * 128, ad, bd, idesc, kk > 0);
+          }
+          umma_commit(b_kvempty(s));
+          umma_commit(b_accfull(acc));
+        }
+      }
+    }
+  } else {
+    // ------------------------------ epilogue -----------------------------------
+    const int e = warp >> 2;            // warpgroup 0 or 1
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane = query row in the block
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    float sc[CAP];
+    uint32_t id[CAP];
+#pragma unroll
+    for (int i = 0; i < CAP; ++i) {
+      sc[i] = -FLT_MAX;
+      id[i] = 0xFFFFFFFFu;
+    }
+    float dsv = -FLT_MAX;
+    uint32_t dav = 0;
+    bool handled_diag = false;
+    const float ps = a.proxy_scale;
+    for (int n0 = 2 * e; n0 < nblk; n0 += 4) {
+      bool stop = false;
+      for (int u = 0; u < 2; ++u) {
+        const int n = n0 + u;
+        if (n >= nblk) break;
+        const int acc = n & 3;
+        if (!wait_bar_warp(b_accfull(acc), (n >> 2) & 1, abort_flag, a.status,
+                           wait_site(kKerSelect, 13 + acc, n))) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tb = tbase + lane_off + acc * 128;
+        const bool diag = (n == J);
+        float cm[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32f(tb + c * 32, v);
+          if (diag) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i > row) v[i] = -FLT_MAX;
+          }
+          cm[c] = max32(v);
+        }
+        const float best = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
+        const int bc = cm[0] == best ? 0 : (cm[1] == best ? 1 : (cm[2] == best ? 2 : 3));
+        const bool need = diag || better(best * ps, (uint32_t)n << 8, sc[CAP - 1], id[CAP - 1]);
+        int arg = 0;
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (__any_sync(0xffffffffu, need && bc == c)) {
+              float v[32];
+              tmem_ld32f(tb + c * 32, v);
+              if (need && bc == c) {
+                int aa = 31;
+#pragma unroll
+                for (int i = 30; i >= 0; --i) {
+                  const bool keep = diag ? (c * 32 + i <= row) : true;
+                  aa = (keep && v[i] == best) ? i : aa;
+                }
+                arg = c * 32 + aa;
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_accempty(acc));
+        if (diag) {
+          dsv = best * ps;
+          dav = ((uint32_t)n << 8) | (uint32_t)arg;
+          handled_diag = true;
+        } else if (need) {
+          list_insert<CAP>(sc, id, best * ps, ((uint32_t)n << 8) | (uint32_t)arg);
+        }
+      }
+      if (stop) break;
+    }
+    // ---- merge warpgroup 1's list into warpgroup 0's ----
+    if (handled_diag) {
+      d_sc[row] = dsv;
+      d_id[row] = dav;
+    }
+    if (e == 1) {
+#pragma unroll
+      for (int i = 0; i < CAP; ++i) {
+        m_sc[i * 128 + row] = sc[i];
+        m_id[i * 128 + row] = id[i];
+      }
+    }
+    named_bar_sync(1, 256);
+    if (e == 0) {
+#pragma unroll
+      for (int i = 0; i < CAP; ++i) {
+        const uint32_t oid = m_id[i * 128 + row];
+        if (oid != 0xFFFFFFFFu) list_insert<CAP>(sc, id, m_sc[i * 128 + row], oid);
+      }
+      dsv = d_sc[row];
+      dav = d_id[row];
+      const int K = a.K;
+      const int nsel = min(J, K - 1);  // off-diagonal blocks kept
+      uint8_t tie = 0;
+      if (J > K - 1 && K >= 2) {
+        float s_km2 = 0.f, s_km1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < CAP; ++i) {
+          if (i == K - 2) s_km2 = sc[i];
+          if (i == K - 1) s_km1 = sc[i];
+        }
+        tie = (s_km2 - s_km1) < kTieBand ? 1 : 0;
+      }
+      // plse over the selection (nsel best + diagonal)
+      float mx = dsv;
+#pragma unroll
+      for (int i = 0; i < CAP; ++i)
+        if (i < nsel) mx = fmaxf(mx, sc[i]);
+      float se = __expf(dsv - mx);
+#pragma unroll
+      for (int i = 0; i < CAP; ++i)
+        if (i < nsel) se += __expf(sc[i] - mx);
+      const float plse_v = mx + __logf(se);
+      // ascending block order of the nsel kept entries (odd-even transposition)
+      uint32_t key[CAP];
+#pragma unroll
+      for (int i = 0; i < CAP; ++i) key[i] = i < nsel ? (id[i] >> 8) : 0xFFFFFFFFu;
+#pragma unroll
+      for (int p = 0; p < CAP; ++p) {
+#pragma unroll
+        for (int i = (p & 1); i + 1 < CAP; i += 2) {
+          const bool sw = key[i] > key[i + 1];
+          const uint32_t k0 = key[i], k1 = key[i + 1], i0 = id[i], i1 = id[i + 1];
+          const float s0 = sc[i], s1 = sc[i + 1];
+          key[i] = sw ? k1 : k0;
+          key[i + 1] = sw ? k0 : k1;
+          id[i] = sw ? i1 : i0;
+          id[i + 1] = sw ? i0 : i1;
+          sc[i] = sw ? s1 : s0;
+          sc[i + 1] = sw ? s0 : s1;
+        }
+      }
+      const int t = qstart + row;
+      if (row < nrows && t < a.T) {
+        const size_t base = ((size_t)t * a.hkv + g) * K;
+#pragma unroll
+        for (int s = 0; s < kMaxTopK; ++s) {
+          if (s >= K) break;
+          int32_t b = -1;
+          float scv = 0.f;
+          uint8_t av = 0;
+#pragma unroll
+          for (int i = 0; i < CAP; ++i)
+            if (i == s && i < nsel) {
+              b = (int32_t)(id[i] >> 8);
+              scv = sc[i];
+              av = (uint8_t)(id[i] & 0xFF);
+            }
+          if (s == nsel) {
+            b = J;
+            scv = dsv;
+            av = (uint8_t)(dav & 0xFF);
+          }
+          a.sel_idx[base + s] = b;
+          a.sel_score[base + s] = scv;
+          a.sel_arg[base + s] = av;
+        }
+        a.plse[(size_t)t * a.hkv + g] = plse_v;
+        a.tie[(size_t)t * a.hkv + g] = tie;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int DP, int CAP>
+cudaError_t launch_sel_t(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
+                         const SelArgs& a, cudaStream_t st) {
+  using C = SelCfg<DP>;
+  const size_t smem = 1024 + (1 + kSelStages) * C::kTileBytes + CAP * 128 * 8 + 128 * 8 +
+                      (2 * kSelStages + 9) * 8 + 16;
+  cudaError_t e = cudaFuncSetAttribute(k_select<DP, CAP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = s.nb_bound * s.hkv;
+  k_select<DP, CAP><<<grid, kSelThreads, smem, st>>>(mq, mk, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_select(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
+                          const uint16_t* q_p, const uint16_t* k_p, int32_t* sel_idx,
+                          float* sel_score, uint8_t* sel_arg, float* plse, uint8_t* tie,
+                          unsigned* status, cudaStream_t st) {
+  CUtensorMap mq, mk;
+  const int sw = s.dp == 64 ? 128 : 64;
+  cudaError_t e;
+  if ((e = make_tmap_3d(&mq, q_p, s.dp, s.hkv, s.T, s.dp, 1, 128, sw)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&mk, k_p, s.dp, s.hkv, s.T, s.dp, 1, 128, sw)) != cudaSuccess) return e;
+  SelArgs a{cu_seqlens, cu_blocks, s.ndoc, s.T, s.hkv, s.K, s.nb_bound, s.proxy_scale,
+            sel_idx,    sel_score, sel_arg, plse,   tie,  status};
+  const int cap = s.K <= 4 ? 4 : (s.K <= 8 ? 8 : 16);
+  if (s.dp == 64) {
+    if (cap == 4) return launch_sel_t<64, 4>(s, mq, mk, a, st);
+    if (cap == 8) return launch_sel_t<64, 8>(s, mq, mk, a, st);
+    return launch_sel_t<64, 16>(s, mq, mk, a, st);
+  }
+  if (cap == 4) return launch_sel_t<32, 4>(s, mq, mk, a, st);
+  if (cap == 8) return launch_sel_t<32, 8>(s, mq, mk, a, st);
+  return launch_sel_t<32, 16>(s, mq, mk, a, st);
+}
+
+}  // namespace msa

@@ -1,0 +1,163 @@
+// Declarations shared by the CUDA translation units of libmsa.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/msa.h"
+#include "ptx.cuh"
+
+namespace msa {
+
+constexpr int kBlock = 128;        // KV block (tokens); also the query tile of the selector
+constexpr int kMaxTopK = 16;       // slot index fits in 4 bits of a regroup entry
+constexpr int kMaxBlocks = 49152;  // KV blocks per batch (regroup counters live in shared memory)
+constexpr int kChunkTokens = 2048; // tokens per regroup chunk
+constexpr int kMaxTokens = 1 << 27;
+// Bounded waits give up after this many SM cycles (about 0.5-1 s at GB300 clocks).
+constexpr long long kWaitCycles = 1000000000ll;
+
+// Where a bounded wait gave up, stored above the status code in the status
+// word: kernel id (4 bits), barrier index (8 bits), tile or block index (12 bits).
+enum : uint32_t { kKerSelect = 1, kKerFwd = 2, kKerBwd = 3 };
+__host__ __device__ constexpr uint32_t wait_site(uint32_t kernel, uint32_t bar, int n) {
+  return kernel | (bar << 4) | ((uint32_t)(n < 0 ? 0 : (n > 4095 ? 4095 : n)) << 12);
+}
+
+// ---------------------------------------------------------------------------
+// device status word (first error wins)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_status(unsigned* status, unsigned code) {
+  atomicCAS(status, 0u, code);
+}
+
+// Waits for phase `parity` of `bar`; gives up (records MSA_ERR_TIMEOUT and
+// raises the CTA's abort flag) after kWaitCycles or as soon as another role of
+// the CTA has aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned* status, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      set_status(status, (uint32_t)MSA_ERR_TIMEOUT | (site << 8));
+      return false;
+    }
+  }
+}
+// Warp-uniform form: every lane waits, the result is the AND over the warp.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, unsigned* status,
+                                              uint32_t site) {
+  const bool ok = wait_bar(bar, parity, abort_flag, status, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// Index of the document holding global token t (cu has ndoc+1 entries).
+__device__ __forceinline__ int doc_of_token(const int32_t* cu, int ndoc, int t) {
+  int lo = 0, hi = ndoc - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+// Index of the document holding global block gb (cu_blocks has ndoc+1 entries).
+__device__ __forceinline__ int doc_of_block(const int32_t* cu_blocks, int ndoc, int gb) {
+  int lo = 0, hi = ndoc - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (cu_blocks[mid] <= gb) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
+// shapes known on the host
+// ---------------------------------------------------------------------------
+struct Shape {
+  int T, ndoc, max_seqlen, hq, hkv, G, d, dp, K;
+  int nb_bound;  // upper bound of KV blocks in the batch: ceil(T/128) + ndoc
+  int nchunks;   // regroup chunks
+  float softmax_scale, proxy_scale, kl_weight;
+};
+
+// Workspace carve-up (byte offsets, 256-byte aligned).
+struct Workspace {
+  size_t cu_blocks, chunk_range, cnt, row_ptr, ent;          // metadata + regroup CSR
+  size_t o_part, lse_part;                                     // forward slot partials
+  size_t dsum, dq_part, kl_part;                               // backward
+  size_t total;
+};
+enum WsKind { kWsSelect = 0, kWsFwd = 1, kWsBwd = 2 };
+Workspace workspace_layout(const Shape& s, WsKind kind);
+
+// ---------------------------------------------------------------------------
+// launchers (return cudaGetLastError() of their launches)
+// ---------------------------------------------------------------------------
+struct TmapEncoder;  // opaque; resolves cuTensorMapEncodeTiled once
+cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid,
+                         uint64_t outer, uint32_t box_inner, uint32_t box_mid, uint32_t box_outer,
+                         int swizzle_bytes);
+
+cudaError_t launch_meta(const Shape& s, const int32_t* cu_seqlens, int32_t* cu_blocks,
+                        unsigned* status, cudaStream_t st);
+cudaError_t launch_select(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
+                          const uint16_t* q_p, const uint16_t* k_p, int32_t* sel_idx,
+                          float* sel_score, uint8_t* sel_arg, float* plse, uint8_t* tie,
+                          unsigned* status, cudaStream_t st);
+cudaError_t launch_regroup(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
+                           const int32_t* sel_idx, int32_t* chunk_range, uint32_t* cnt,
+                           int32_t* row_ptr, uint32_t* ent, unsigned* status, cudaStream_t st);
+cudaError_t launch_fwd(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
+                       const int32_t* row_ptr, const uint32_t* ent, const uint16_t* q,
+                       const uint16_t* k, const uint16_t* v, float* o_part, float* lse_part,
+                       unsigned* status, cudaStream_t st);
+cudaError_t launch_fwd_merge(const Shape& s, const int32_t* cu_seqlens, const float* o_part,
+                             const float* lse_part, uint16_t* o, uint16_t* o_res, float* lse,
+                             float* mass, cudaStream_t st);
+cudaError_t launch_bwd_pre(const Shape& s, const uint16_t* o, const uint16_t* o_res,
+                           const uint16_t* dO, float* dsum, cudaStream_t st);
+cudaError_t launch_bwd(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
+                       const int32_t* row_ptr, const uint32_t* ent, const uint16_t* q,
+                       const uint16_t* k, const uint16_t* v, const uint16_t* q_p,
+                       const uint16_t* dO, const float* lse, const float* dsum, const float* mass,
+                       const float* sel_score, const uint8_t* sel_arg, const float* plse,
+                       float* dq_part, float* dk, float* dv, float* dk_p, unsigned* status,
+                       cudaStream_t st);
+cudaError_t launch_bwd_reduce(const Shape& s, const int32_t* cu_seqlens, const float* dq_part,
+                              const int32_t* sel_idx, const float* sel_score,
+                              const uint8_t* sel_arg, const float* plse, const float* mass,
+                              const uint16_t* k_p, float* dq, float* dq_p, double* kl_part,
+                              double* kl_loss, cudaStream_t st);
+int bwd_reduce_blocks(const Shape& s);
+
+}  // namespace msa

@@ -1,0 +1,63 @@
+"""One MSA training step through the C ABI: proxy select -> forward -> backward.
+
+The three calls run back to back on one stream and share one caller-owned
+workspace (the largest of the three sizes): the forward's slot partials are
+dead once its merge has run, so the backward reuses the same bytes.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (allocate_outputs, make_params, msa_bwd, msa_bwd_workspace_size, msa_fwd,
+               msa_fwd_workspace_size, msa_proxy_select, msa_select_workspace_size, workspace)
+
+
+def params_for(cu_seqlens_host, hq, hkv, d, dp, top_k, **kw):
+    lens = [int(b) - int(a) for a, b in zip(cu_seqlens_host[:-1], cu_seqlens_host[1:])]
+    return make_params(int(cu_seqlens_host[-1]), len(lens), max(lens) if lens else 0, hq, hkv, d,
+                       dp, top_k, **kw)
+
+
+def workspace_bytes(params) -> int:
+    return max(msa_select_workspace_size(params), msa_fwd_workspace_size(params),
+               msa_bwd_workspace_size(params))
+
+
+class MSAStep:
+    """Holds outputs and workspace for repeated steps at one shape."""
+
+    def __init__(self, params, device="cuda"):
+        self.params = params
+        self.out = allocate_outputs(params, device)
+        self.ws = workspace(workspace_bytes(params), device)
+
+    def select(self, inp, stream=None):
+        o = self.out
+        msa_proxy_select(self.params, inp["cu_seqlens"], inp["q_p"], inp["k_p"], o["sel_idx"],
+                         o["sel_score"], o["sel_arg"], o["plse"], o["tie"], self.ws, stream)
+
+    def forward(self, inp, stream=None):
+        o = self.out
+        msa_fwd(self.params, inp["cu_seqlens"], inp["q"], inp["k"], inp["v"], o["sel_idx"], o["o"],
+                o["o_res"], o["lse"], o["mass"], self.ws, stream)
+
+    def backward(self, inp, stream=None):
+        o = self.out
+        msa_bwd(self.params, inp["cu_seqlens"], inp["q"], inp["k"], inp["v"], inp["q_p"],
+                inp["k_p"], o["o"], o["o_res"], o["lse"], o["mass"], inp["dO"], o["sel_idx"],
+                o["sel_score"],
+                o["sel_arg"], o["plse"], o["dq"], o["dk"], o["dv"], o["dq_p"], o["dk_p"],
+                o["kl_loss"], self.ws, stream)
+
+    def __call__(self, inp, stream=None):
+        self.select(inp, stream)
+        self.forward(inp, stream)
+        self.backward(inp, stream)
+        return self.out
+
+
+def run_step(params, inp, device="cuda") -> dict:
+    step = MSAStep(params, device)
+    out = step(inp)
+    torch.cuda.synchronize()
+    return out

@@ -303,14 +303,15 @@ def msa_reference(inputs: dict, prm: OracleParams, sel_override=None, arg_overri
 # the same steps for one query token (sampled rows of long sequences)
 # ---------------------------------------------------------------------------
 def row_reference(inputs: dict, prm: OracleParams, t: int, sel_override=None, arg_override=None,
-                  contributions: bool = False) -> dict:
+                  contributions: bool = False, groups=None) -> dict:
     """Forward + backward quantities of one token t (all heads, all groups).
 
     Row-local outputs: sel (own selection), gap, sel_score, plse, o, lse, mass,
     p, kl, dq, dq_p.  With contributions=True also the row's additive
     contributions to dk / dv (per group: key indices and [n, d] rows) and to
     dk_p.  inputs may be torch tensors (bf16) or numpy arrays; only the rows
-    that token t can see are upcast.
+    that token t can see are upcast.  `groups` restricts the work to some KV
+    groups (the others' entries stay zero).
     """
     cu = _i64(inputs["cu_seqlens"])
     doc = int(np.searchsorted(cu, t, side="right") - 1)
@@ -321,7 +322,7 @@ def row_reference(inputs: dict, prm: OracleParams, t: int, sel_override=None, ar
     q_t = _f64(inputs["q"][t])  # [Hq, d]
     do_t = _f64(inputs["dO"][t])
     qp_t = _f64(inputs["q_p"][t])  # [Hkv, dp]
-    kp = _f64(inputs["k_p"][s0:t + 1])  # [i+1, Hkv, dp]
+    kp = _f64(inputs["k_p"][s0:t + 1])  # [i+1, Hkv, dp] (a view when k_p is fp64 numpy)
     res = dict(sel=np.full((prm.hkv, K), -1, dtype=np.int64), gap=np.full(prm.hkv, math.inf),
                sel_score=np.zeros((prm.hkv, K)), sel_arg=np.zeros((prm.hkv, K), dtype=np.int64),
                own_arg=np.zeros((prm.hkv, K), dtype=np.int64),
@@ -329,7 +330,7 @@ def row_reference(inputs: dict, prm: OracleParams, t: int, sel_override=None, ar
                mass=np.zeros((prm.hkv, K)), p=np.zeros((prm.hkv, K)), kl=np.zeros(prm.hkv),
                dq=np.zeros((prm.hq, prm.d)), dq_p=np.zeros((prm.hkv, prm.dp)),
                pooled=np.full((prm.hkv, j + 1), NEG_INF), contrib=[])
-    for g in range(prm.hkv):
+    for g in (range(prm.hkv) if groups is None else groups):
         s = prm.proxy_scale * (kp[:, g, :] @ qp_t[g])  # keys 0..i
         spad = np.full((j + 1) * B, NEG_INF)
         spad[: i + 1] = s

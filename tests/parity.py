@@ -1,0 +1,65 @@
+"""Shared comparison helpers for the GPU-vs-oracle parity tests.
+
+Tolerances (floating point, bf16 inputs, fp32 accumulation on the GPU):
+cosine similarity >= 0.9995 and max |gpu - oracle| <= 2e-2 for O, dQ, dK, dV,
+dq_p, dk_p; the KL loss to 1e-3 relative.  Integer outputs (block indices,
+argmax offsets, regroup lists) are compared exactly, except where the oracle's
+(k-1)-th and k-th best pooled scores lie within 1e-3 of each other: there the
+differing blocks must all sit inside that tie band.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+COS_MIN = 0.9995
+ABS_MAX = 2e-2
+TIE_BAND = 1e-3
+KL_RTOL = 1e-3
+
+
+def cos(a, b) -> float:
+    a = np.asarray(a, np.float64).ravel()
+    b = np.asarray(b, np.float64).ravel()
+    na, nb = np.linalg.norm(a), np.linalg.norm(b)
+    if na == 0 and nb == 0:
+        return 1.0
+    return float(a @ b / (na * nb + 1e-300))
+
+
+def assert_close(name, gpu, ref, cos_min=COS_MIN, abs_max=ABS_MAX):
+    g = np.asarray(gpu, np.float64)
+    r = np.asarray(ref, np.float64)
+    assert g.shape == r.shape, (name, g.shape, r.shape)
+    assert np.isfinite(g).all(), f"{name}: non-finite GPU values"
+    e = float(np.abs(g - r).max()) if g.size else 0.0
+    if g.size == 0 or float(np.abs(r).max()) < 1e-9:
+        # an identically-zero quantity (e.g. the proxy gradient when every row
+        # keeps a single block): the cosine is undefined, only the abs bound applies
+        assert e <= abs_max, f"{name}: max-abs {e:.3e} (<= {abs_max}) on a zero reference"
+        return 1.0, e
+    c = cos(g, r)
+    assert c >= cos_min and e <= abs_max, f"{name}: cos {c:.6f} (>= {cos_min}), max-abs {e:.3e} (<= {abs_max})"
+    return c, e
+
+
+def check_selection_row(gpu_sel, own_sel, pooled, j, k):
+    """One (row, group): GPU and oracle block lists must agree, or differ only in
+    blocks whose oracle pooled score is within TIE_BAND of the selection boundary.
+    Returns True when the row is an excused tie."""
+    gpu_sel = [int(x) for x in gpu_sel]
+    own_sel = [int(x) for x in own_sel]
+    if gpu_sel == own_sel:
+        return False
+    # structure: ascending, diagonal last, -1 padding
+    n_off = min(j, k - 1)
+    assert gpu_sel[n_off] == j and all(x == -1 for x in gpu_sel[n_off + 1:]), gpu_sel
+    assert gpu_sel[:n_off] == sorted(set(gpu_sel[:n_off])), gpu_sel
+    cand = np.asarray(pooled[:j], np.float64)
+    srt = np.sort(cand)[::-1]
+    lo = srt[k - 1] if len(srt) > k - 1 else -np.inf   # best excluded
+    hi = srt[k - 2]                                      # worst included
+    assert hi - lo < TIE_BAND, f"selection differs outside the tie band: {gpu_sel} vs {own_sel}"
+    diff = set(gpu_sel[:n_off]) ^ set(own_sel[:n_off])
+    for b in diff:
+        assert lo - TIE_BAND <= cand[b] <= hi + TIE_BAND, (b, cand[b], lo, hi)
+    return True

@@ -1,0 +1,189 @@
+"""GPU (CUDA path through the C ABI) against the fp64 CPU oracle, every row.
+
+Workloads: the 1024-token tiny step, the 32768-token varlen batch, and small
+shapes for the edge cases: ragged document tails, one-token and one-block
+documents, top-k covering every block (dense limit), k = 1, and G = 1 / 2 / 8.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import OracleParams, msa_reference
+from parity import KL_RTOL, assert_close, check_selection_row
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, inp_cpu):
+    from block_sparse_attention_proxy_gb300 import msa_get_device_status
+    from block_sparse_attention_proxy_gb300.step import params_for, run_step
+
+    dev = {k: v.cuda() for k, v in inp_cpu.items()}
+    prm = params_for(inp_cpu["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k)
+    out = run_step(prm, dev)
+    assert msa_get_device_status() == 0
+    return {k: v.cpu() for k, v in out.items()}
+
+
+def _check_all(w, inp, g):
+    prm = OracleParams(w.hq, w.hkv, w.d, w.dp, w.top_k)
+    ref = msa_reference(inp, prm, sel_override=g["sel_idx"], arg_override=g["sel_arg"])
+    sel = g["sel_idx"].numpy()
+    own = ref["own_sel_idx"]
+    ties = 0
+    pooled = dict(ref["pooled"])
+    cu = inp["cu_seqlens"].tolist()
+    for a, b in zip(cu[:-1], cu[1:]):
+        if b == a:
+            continue
+        S = pooled[a]
+        for i in range(b - a):
+            for gg in range(w.hkv):
+                ties += check_selection_row(sel[a + i, gg], own[a + i, gg], S[i, gg], i // 128,
+                                            w.top_k)
+    # where the selections agree, the argmax key agrees unless within the tie band
+    same = (sel == own).all(-1)
+    arg_g = g["sel_arg"].numpy().astype(np.int64)
+    arg_o = ref["own_sel_arg"]
+    bad = same[..., None] & (arg_g != arg_o) & (sel >= 0)
+    for t, gg, s in zip(*np.nonzero(bad)):
+        a = max(x for x in cu[:-1] if x <= t)
+        i = t - a
+        bblk = sel[t, gg, s]
+        sc = (inp["q_p"][t, gg].double() @ inp["k_p"][a + bblk * 128 + arg_g[t, gg, s], gg].double())
+        assert abs(float(sc) - ref["sel_score"][t, gg, s]) < 1e-3, (t, gg, s)
+    # pooled scores and proxy normaliser
+    assert_close("sel_score", g["sel_score"].numpy(), ref["sel_score"], abs_max=1e-3)
+    assert_close("plse", g["plse"].numpy(), ref["plse"], abs_max=1e-3)
+    # attention outputs and gradients (oracle on the GPU's selection)
+    assert_close("o", g["o"].float().numpy(), ref["o"])
+    assert_close("lse", g["lse"].numpy(), ref["lse"], abs_max=1e-2)
+    assert_close("mass", g["mass"].numpy(), ref["mass"], abs_max=5e-3)
+    for n in ("dq", "dk", "dv", "dq_p", "dk_p"):
+        assert_close(n, g[n].numpy(), ref[n])
+    kl = float(g["kl_loss"][0])
+    assert abs(kl - ref["kl_loss"]) <= KL_RTOL * max(1.0, abs(ref["kl_loss"])), (kl, ref["kl_loss"])
+    return ties
+
+
+def test_tiny_workload():
+    w = synth.workload("tiny")
+    inp = synth.make_inputs(w)
+    g = _run(w, inp)
+    _check_all(w, inp, g)
+
+
+def test_varlen_workload():
+    w = synth.workload("varlen")
+    inp = synth.make_inputs(w)
+    g = _run(w, inp)
+    _check_all(w, inp, g)
+
+
+EDGE = [
+    # (doc lengths, hq, hkv, d, dp, k, structured)
+    ([1, 129, 300, 128, 77, 513], 8, 2, 128, 64, 3, False),   # ragged tails, 1-token doc
+    ([600], 4, 1, 64, 32, 16, False),                          # k covers every block
+    ([700, 260], 2, 2, 64, 64, 2, False),                      # G = 1
+    ([900], 8, 1, 128, 32, 5, False),                          # G = 8
+    ([400, 1], 4, 2, 128, 64, 1, False),                       # k = 1: diagonal only
+    ([2048], 8, 4, 128, 64, 4, True),                          # G = 2, structured keys
+    ([1280, 1024], 4, 1, 64, 64, 6, True),                     # d = 64, dp = 64
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=[f"edge{i}" for i in range(len(EDGE))])
+def test_edge_shapes(case):
+    lens, hq, hkv, d, dp, k, structured = case
+    w = synth.custom(lens, hq, hkv, d, dp, k, seed=100 + len(lens) + hq, structured=structured)
+    inp = synth.make_inputs(w)
+    g = _run(w, inp)
+    _check_all(w, inp, g)
+
+
+def test_deterministic():
+    w = synth.custom([3000, 1100], 8, 2, 128, 64, 4, seed=5, structured=True)
+    inp = synth.make_inputs(w)
+    a = _run(w, inp)
+    b = _run(w, inp)
+    for n in a:
+        assert torch.equal(a[n], b[n]), n
+
+
+def test_regroup_matches_stable_sort():
+    """The CSR built inside the library lists, per (group, block), exactly the
+    (token, slot) pairs whose selection chose that block off the diagonal, in
+    ascending token order (checked through the forward's use of it: every slot
+    partial of every row is reached, so O matches the oracle; and directly here
+    by reconstructing the lists from sel_idx with a CPU stable sort)."""
+    import block_sparse_attention_proxy_gb300 as m
+    from block_sparse_attention_proxy_gb300.step import params_for
+
+    w = synth.custom([1500, 900, 1], 8, 2, 128, 64, 5, seed=9)
+    inp = synth.make_inputs(w)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    prm = params_for(inp["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k)
+    out = m.allocate_outputs(prm)
+    ws = m.workspace(m.msa_fwd_workspace_size(prm))
+    m.msa_proxy_select(prm, dev["cu_seqlens"], dev["q_p"], dev["k_p"], out["sel_idx"],
+                       out["sel_score"], out["sel_arg"], out["plse"], out["tie"], ws)
+    m.msa_fwd(prm, dev["cu_seqlens"], dev["q"], dev["k"], dev["v"], out["sel_idx"], out["o"],
+              out["o_res"], out["lse"], out["mass"], ws)
+    torch.cuda.synchronize()
+    # workspace layout (see the library's workspace carve-up): cu_blocks, chunk_range, cnt, row_ptr, ent
+    T, K, hkv = w.total_tokens, w.top_k, w.hkv
+    ndoc = w.num_docs
+    nbs = (T + 127) // 128 + ndoc
+    nch = (T + 2047) // 2048
+
+    def al(x):
+        return (x + 255) // 256 * 256
+
+    off_rowptr = al(al(al((ndoc + 2) * 4) + 2 * nch * 4) + nch * hkv * nbs * 4)
+    off_ent = al(off_rowptr + (hkv * nbs + 1) * 4)
+    wsc = ws.cpu()
+    row_ptr = wsc[off_rowptr:off_rowptr + (hkv * nbs + 1) * 4].view(torch.int32).numpy()
+    ent = wsc[off_ent:off_ent + T * hkv * (K - 1) * 4].view(torch.int32).numpy().view(np.uint32)
+    sel = out["sel_idx"].cpu().numpy()
+    cu = inp["cu_seqlens"].tolist()
+    cu_blocks = [0]
+    for a, b in zip(cu[:-1], cu[1:]):
+        cu_blocks.append(cu_blocks[-1] + (b - a + 127) // 128)
+    want = {}
+    for d_, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        for t in range(a, b):
+            j = (t - a) // 128
+            for gg in range(hkv):
+                for s in range(min(j, K - 1)):
+                    key = (gg, cu_blocks[d_] + int(sel[t, gg, s]))
+                    want.setdefault(key, []).append((t << 4) | s)
+    for gg in range(hkv):
+        for gb in range(cu_blocks[-1]):
+            lst = ent[row_ptr[gg * nbs + gb]:row_ptr[gg * nbs + gb + 1]].tolist()
+            assert lst == want.get((gg, gb), []), (gg, gb)
+
+
+def test_device_check_on_malformed_inputs():
+    """Malformed cu_seqlens / selection are caught on the device (status word),
+    after in-bounds handling; nothing faults."""
+    import block_sparse_attention_proxy_gb300 as m
+    from block_sparse_attention_proxy_gb300.step import MSAStep
+
+    w = synth.custom([700, 324], 4, 2, 64, 32, 3, seed=3)
+    inp = synth.make_inputs(w)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    prm = m.make_params(1024, 2, 700, 4, 2, 64, 32, 3)
+    step = MSAStep(prm)
+    assert m.msa_get_device_status() == 0
+    bad = dict(dev)
+    bad["cu_seqlens"] = torch.tensor([0, 800, 1024], dtype=torch.int32, device="cuda")  # > max_seqlen
+    step.select(bad)
+    assert m.msa_get_device_status() == 6
+    step.select(dev)
+    assert m.msa_get_device_status() == 0
+    sel = step.out["sel_idx"].clone()
+    sel[650, 1, 0] = 7  # a block after the row's own block
+    step.out["sel_idx"].copy_(sel)
+    step.forward(dev)
+    assert m.msa_get_device_status() == 6
