@@ -21,7 +21,7 @@ from ._abi import EXPORTS, LIB_PATH, MSA_OK, MsaError, MsaParams, STATUS_NAMES, 
 
 __all__ = [
     "MsaError", "MsaParams", "make_params", "msa_select_workspace_size", "msa_fwd_workspace_size",
-    "msa_bwd_workspace_size", "msa_proxy_select", "msa_fwd", "msa_bwd", "msa_get_device_status",
+    "msa_bwd_workspace_size", "msa_proxy_select", "msa_proxy_select_noalloc", "msa_fwd", "msa_bwd", "msa_get_device_status",
     "msa_last_status_word", "msa_launch_count", "msa_set_profile_events", "msa_status_string", "allocate_outputs", "workspace", "EXPORTS", "LIB_PATH", "load",
 ]
 
@@ -75,6 +75,16 @@ def msa_proxy_select(params, cu_seqlens, q_p, k_p, sel_idx, sel_score, sel_arg, 
                                    _ptr(sel_idx), _ptr(sel_score), _ptr(sel_arg), _ptr(plse),
                                    _ptr(tie), _ptr(ws), ws.numel() * ws.element_size(),
                                    _stream(stream)), "msa_proxy_select")
+
+
+def msa_proxy_select_noalloc(params, cu_seqlens, q_p, k_p, sel_idx, sel_score, sel_arg, plse, tie,
+                             stream=None) -> None:
+    """msa_proxy_select for callers that cannot allocate: no workspace argument,
+    the scratch is a static device array inside the library (see include/msa.h)."""
+    _check(load().msa_proxy_select_noalloc(ctypes.byref(params), _ptr(cu_seqlens), _ptr(q_p),
+                                           _ptr(k_p), _ptr(sel_idx), _ptr(sel_score),
+                                           _ptr(sel_arg), _ptr(plse), _ptr(tie), _stream(stream)),
+           "msa_proxy_select_noalloc")
 
 
 def msa_fwd(params, cu_seqlens, q, k, v, sel_idx, o, o_res, lse, mass, ws, stream=None) -> None:

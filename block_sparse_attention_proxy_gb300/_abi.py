@@ -24,6 +24,7 @@ EXPORTS = (
     "msa_fwd_workspace_size",
     "msa_bwd_workspace_size",
     "msa_proxy_select",
+    "msa_proxy_select_noalloc",
     "msa_fwd",
     "msa_bwd",
     "msa_get_device_status",
@@ -79,6 +80,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         getattr(lib, name).restype = sz
     lib.msa_proxy_select.argtypes = [P] + [vp] * 8 + [vp, sz, vp]
     lib.msa_proxy_select.restype = i32
+    lib.msa_proxy_select_noalloc.argtypes = [P] + [vp] * 8 + [vp]
+    lib.msa_proxy_select_noalloc.restype = i32
     lib.msa_fwd.argtypes = [P] + [vp] * 9 + [vp, sz, vp]
     lib.msa_fwd.restype = i32
     lib.msa_bwd.argtypes = [P] + [vp] * 21 + [vp, sz, vp]

@@ -12,10 +12,11 @@ namespace msa {
 __device__ unsigned int g_msa_status = 0;
 
 namespace {
-
 constexpr int kMaxDevices = 64;
 unsigned* g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
+
+}  // namespace
 
 // Address of this device's status word (resolved once per device).
 cudaError_t status_ptr(unsigned** out) {
@@ -34,6 +35,8 @@ cudaError_t status_ptr(unsigned** out) {
   return cudaSuccess;
 }
 
+namespace {
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -44,6 +47,12 @@ std::once_flag g_encode_once;
 std::atomic<uint64_t> g_launches{0};
 cudaEvent_t g_prof_start[4] = {}, g_prof_stop[4] = {};
 
+}  // namespace
+
+void add_launches(uint64_t n) { g_launches += n; }
+
+namespace {
+
 // Records the profiling event of kernel `which` (if one is set) on `st`.
 cudaError_t prof_mark(int which, bool start, cudaStream_t st) {
   cudaEvent_t e = start ? g_prof_start[which] : g_prof_stop[which];
@@ -53,6 +62,8 @@ cudaError_t prof_mark(int which, bool start, cudaStream_t st) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
 
 msa_status check_params(const msa_params* p, Shape* s) {
   if (!p) return MSA_ERR_INVALID_ARG;
@@ -90,6 +101,8 @@ msa_status check_params(const msa_params* p, Shape* s) {
   s->kl_weight = p->kl_weight;
   return MSA_OK;
 }
+
+namespace {
 
 msa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
 

@@ -120,6 +120,13 @@ struct Workspace {
 enum WsKind { kWsSelect = 0, kWsFwd = 1, kWsBwd = 2 };
 Workspace workspace_layout(const Shape& s, WsKind kind);
 
+// Host-side parameter checks shared by the entry points (fills `s` on MSA_OK).
+msa_status check_params(const msa_params* p, Shape* s);
+// Address of the current device's status word.
+cudaError_t status_ptr(unsigned** out);
+// Adds to the process-wide count of launched kernels (msa_launch_count).
+void add_launches(uint64_t n);
+
 // ---------------------------------------------------------------------------
 // launchers (return cudaGetLastError() of their launches)
 // ---------------------------------------------------------------------------

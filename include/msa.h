@@ -151,6 +151,31 @@ msa_status msa_bwd(const msa_params* params, const int32_t* cu_seqlens, const ui
                    double* kl_loss, void* workspace, size_t workspace_bytes, msa_stream_t stream);
 
 /*
+ * msa_proxy_select without a workspace, for callers that cannot allocate
+ * device memory.  Some host programs have no way to hand the library a
+ * buffer: all device memory belongs to another component's allocator that
+ * exposes no raw pointers, or the call sits on a path where cudaMalloc (which
+ * can synchronise the whole device) is not allowed.  This entry point takes
+ * the same inputs and writes the same outputs as msa_proxy_select; its only
+ * scratch, the per-document block prefix, lives in a static device array of
+ * 16384 int32 (64 KB) that every GPU loading the library keeps until the
+ * process exits.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.  Limits and caveats:
+ *   - batches of more than 16382 documents return MSA_ERR_WORKSPACE;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current, so make that first
+ *     call before any stream capture;
+ *   - all calls share the one array: calls that overlap on the GPU (for
+ *     example on two streams without ordering between them) race on it.
+ *     Each call writes every entry it reads, so no clearing is needed.
+ * The pages have no counterpart of this entry point.
+ */
+msa_status msa_proxy_select_noalloc(const msa_params* params, const int32_t* cu_seqlens,
+                                    const uint16_t* q_p, const uint16_t* k_p, int32_t* sel_idx,
+                                    float* sel_score, uint8_t* sel_arg, float* plse, uint8_t* tie,
+                                    msa_stream_t stream);
+
+/*
  * Synchronises `stream`, returns the device status word of the current device
  * (MSA_OK, MSA_ERR_TIMEOUT or MSA_ERR_DEVICE_CHECK; the first error recorded
  * wins) and resets it to MSA_OK.  Returns MSA_ERR_CUDA if the stream itself
