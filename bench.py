@@ -356,36 +356,9 @@ def run_ours(args):
                                           unit=models[k]["unit"]) for k in kern_ms}
 
     # ---- end to end through the C ABI with host buffers ----
-    names_in = ("q", "k", "v", "q_p", "k_p", "dO", "cu_seqlens")
-    host_in = {n: inp[n].to("cpu").pin_memory() for n in names_in}
-    names_out = ("o", "dq", "dk", "dv", "dq_p", "dk_p", "kl_loss")
-    host_out = {n: torch.empty_like(step.out[n], device="cpu").pin_memory() for n in names_out}
-    dev_in = {n: torch.empty_like(inp[n]) for n in names_in}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-
-    def e2e_step():
-        for n in names_in:
-            dev_in[n].copy_(host_in[n], non_blocking=True)
-        step(dev_in)
-        for n in names_out:
-            host_out[n].copy_(step.out[n], non_blocking=True)
-
-    for _ in range(max(1, W)):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = E(), E()
-    e0.record()
-    for _ in range(K):
-        e2e_step()
-    e1.record()
-    torch.cuda.synchronize()
-    barrier(world)
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / K, world)
-    e2e = dict(value=round(fl * world / ms_e2e / 1e9, 3), unit=UNIT,
-               ms_per_step=round(ms_e2e, 3), h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-               tokens_per_s=round(w.total_tokens * world / ms_e2e * 1e3, 1))
+    e2e = None
+    if args.e2e:
+        e2e = run_e2e(w, inp, step, fl, K, W, world)
 
     dense = dense_sdpa(w, inp) if (args.dense and rank == 0) else None
     cpu = None
@@ -416,6 +389,44 @@ def run_ours(args):
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+def run_e2e(w, inp, step, fl, K, W, world) -> dict:
+    """The same metric end to end through the C ABI: every step copies its
+    inputs from pinned host memory and all its outputs back inside the timed
+    region."""
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    names_in = ("q", "k", "v", "q_p", "k_p", "dO", "cu_seqlens")
+    host_in = {n: inp[n].to("cpu").pin_memory() for n in names_in}
+    names_out = ("o", "dq", "dk", "dv", "dq_p", "dk_p", "kl_loss")
+    host_out = {n: torch.empty_like(step.out[n], device="cpu").pin_memory() for n in names_out}
+    dev_in = {n: torch.empty_like(inp[n]) for n in names_in}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for n in names_in:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        step(dev_in)
+        for n in names_out:
+            host_out[n].copy_(step.out[n], non_blocking=True)
+
+    for _ in range(max(1, W)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = E(), E()
+    e0.record()
+    for _ in range(K):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / K, world)
+    return dict(value=round(fl * world / ms_e2e / 1e9, 3), unit=UNIT,
+               ms_per_step=round(ms_e2e, 3), h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+               tokens_per_s=round(w.total_tokens * world / ms_e2e * 1e3, 1))
+
 
 
 # ---------------------------------------------------------------------------
@@ -478,6 +489,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--no-dense", dest="dense", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false",
+                    help="skip the end-to-end leg (profiling runs only)")
     ap.add_argument("--cpu-rows", type=int, default=24)
     ap.add_argument("--ref-rows", type=int, default=4)
     args = ap.parse_args()

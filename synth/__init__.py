@@ -13,6 +13,8 @@ Workloads (shapes, value distributions, structure):
            k and k_p carry a shared rank-8 component, seed 2
   512k     as 128k with 524288 tokens, seed 3
   1m       as 128k with 1048576 tokens, seed 4
+  8k       as 128k with 8192 tokens, seed 5 (a profiling-size case of the same kernels:
+           its inputs still exceed L2, its workspace stays near 1.5 GB)
 
 Recipe (all draws fp32 from one torch.Generator seeded with the workload
 seed, in this order, then rounded to bf16):
@@ -88,10 +90,12 @@ def workload(name: str) -> Workload:
         return Workload("512k", (524288,), 32, 8, 128, 64, 16, 3, True)
     if name == "1m":
         return Workload("1m", (1048576,), 32, 8, 128, 64, 16, 4, True)
+    if name == "8k":
+        return Workload("8k", (8192,), 32, 8, 128, 64, 16, 5, True)
     raise KeyError(name)
 
 
-WORKLOADS = ("tiny", "varlen", "128k", "512k", "1m")
+WORKLOADS = ("tiny", "varlen", "128k", "512k", "1m", "8k")
 
 
 def custom(doc_lengths, hq, hkv, d, dp, top_k, seed, structured=False, block=BLOCK) -> Workload:
