@@ -138,6 +138,9 @@ Workspace workspace_layout(const Shape& s, WsKind kind) {
     w.dsum = take((size_t)s.T * s.hq * 4);
     w.dq_part = take((size_t)s.T * s.hq * s.K * s.d * 4);
     w.kl_part = take((size_t)bwd_reduce_blocks(s) * 8 + 8);
+    // one record per list entry (diagonal + gathered) of every (group, block),
+    // plus one tile of padding read by the last tile's bulk copy
+    w.rec = take(((size_t)s.T * s.hkv * s.K + 64) * bwd_rec_bytes(s.G));
   }
   w.total = off;
   return w;
@@ -299,12 +302,12 @@ msa_status msa_bwd(const msa_params* p, const int32_t* cu_seqlens, const uint16_
                          status, cs));
   MSA_TRY(launch_bwd_pre(s, o, o_res, dO, dsum, cs));
   MSA_TRY(prof_mark(3, true, cs));
-  MSA_TRY(launch_bwd(s, cu_seqlens, cu_blocks, row_ptr, ent, q, k, v, q_p, dO, lse, dsum, mass,
-                     sel_score, sel_arg, plse, dq_part, dk, dv, dk_p, status, cs));
+  MSA_TRY(launch_bwd(s, cu_seqlens, cu_blocks, row_ptr, ent, base + w.rec, q, k, v, q_p, dO, lse,
+                     dsum, mass, sel_score, sel_arg, plse, dq_part, dk, dv, dk_p, status, cs));
   MSA_TRY(prof_mark(3, false, cs));
   MSA_TRY(launch_bwd_reduce(s, cu_seqlens, dq_part, sel_idx, sel_score, sel_arg, plse, mass, k_p,
                             dq, dq_p, kl_part, kl_loss, cs));
-  g_launches += 9;
+  g_launches += 10;
   return MSA_OK;
 }
 

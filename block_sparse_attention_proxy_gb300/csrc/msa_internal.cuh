@@ -100,6 +100,11 @@ __device__ __forceinline__ int doc_of_block(const int32_t* cu_blocks, int ndoc, 
   return lo;
 }
 
+// Bytes of one backward list-entry record for a group of G heads: a 16-byte
+// header {token, slot, argmax offset, proxy coefficient} and G (LSE, D) pairs,
+// padded to a multiple of 16 bytes.
+__host__ __device__ constexpr int bwd_rec_bytes(int G) { return 16 + ((8 * G + 15) / 16) * 16; }
+
 // ---------------------------------------------------------------------------
 // shapes known on the host
 // ---------------------------------------------------------------------------
@@ -114,7 +119,7 @@ struct Shape {
 struct Workspace {
   size_t cu_blocks, chunk_range, cnt, row_ptr, ent;          // metadata + regroup CSR
   size_t o_part, lse_part;                                     // forward slot partials
-  size_t dsum, dq_part, kl_part;                               // backward
+  size_t dsum, dq_part, kl_part, rec;                          // backward
   size_t total;
 };
 enum WsKind { kWsSelect = 0, kWsFwd = 1, kWsBwd = 2 };
@@ -154,12 +159,12 @@ cudaError_t launch_fwd_merge(const Shape& s, const int32_t* cu_seqlens, const fl
 cudaError_t launch_bwd_pre(const Shape& s, const uint16_t* o, const uint16_t* o_res,
                            const uint16_t* dO, float* dsum, cudaStream_t st);
 cudaError_t launch_bwd(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
-                       const int32_t* row_ptr, const uint32_t* ent, const uint16_t* q,
-                       const uint16_t* k, const uint16_t* v, const uint16_t* q_p,
-                       const uint16_t* dO, const float* lse, const float* dsum, const float* mass,
-                       const float* sel_score, const uint8_t* sel_arg, const float* plse,
-                       float* dq_part, float* dk, float* dv, float* dk_p, unsigned* status,
-                       cudaStream_t st);
+                       const int32_t* row_ptr, const uint32_t* ent, uint8_t* rec,
+                       const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const uint16_t* q_p, const uint16_t* dO, const float* lse,
+                       const float* dsum, const float* mass, const float* sel_score,
+                       const uint8_t* sel_arg, const float* plse, float* dq_part, float* dk,
+                       float* dv, float* dk_p, unsigned* status, cudaStream_t st);
 cudaError_t launch_bwd_reduce(const Shape& s, const int32_t* cu_seqlens, const float* dq_part,
                               const int32_t* sel_idx, const float* sel_score,
                               const uint8_t* sel_arg, const float* plse, const float* mass,
