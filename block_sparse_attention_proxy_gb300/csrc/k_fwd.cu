@@ -8,15 +8,19 @@
 //   * first the block's own queries (the diagonal slot, causal inside the block),
 //   * then the gathered queries from the regroup CSR (full block, no mask).
 // Per tile: S = Q K^T on tcgen05 into TMEM, exact softmax over the block's 128
-// keys (one TMEM lane = one row), P to shared memory as two bf16 operands
-// (hi = bf16(P), lo = bf16(P - hi), so O keeps ~16 mantissa bits of P; the
-// backward's D = rowsum(dO * O) needs that), O = P_hi V + P_lo V into TMEM,
-// and the normalised partial O_slot and lse_slot (both fp32) are written per
-// (token, head, slot).  The merge kernel combines the slots by log-sum-exp.
+// keys (one TMEM lane = one row).  P goes back into the same TMEM columns as
+// two bf16 operands, hi = bf16(P) and lo = bf16(P - hi) (16 hi and 16 lo
+// columns in place of each 32 score columns, so no unread score is
+// overwritten), and O = P_hi V + P_lo V reads P straight from TMEM; O keeps
+// ~16 mantissa bits of P, which the backward's D = rowsum(dO * O) needs.  The
+// normalised partial O_slot and lse_slot (both fp32) are written per (token,
+// head, slot); the merge kernel combines the slots by log-sum-exp.
 //
-// Roles (192 threads): warps 0-3 softmax/epilogue, warp 4 TMA producer,
-// warp 5 MMA issuer.  Two Q buffers, two S and two O accumulators, one P buffer
-// (the epilogue rewrites P only after the previous P V has completed).
+// Roles (320 threads): two softmax warpgroups (warps 0-3 and 4-7) take
+// alternate tiles through two S/O accumulator pairs, so one warpgroup's
+// softmax overlaps the other's P V product and O stores; warp 8 is the TMA
+// producer (regroup entries read one tile ahead, four Q stages); warp 9 issues
+// the MMAs.
 #include <cfloat>
 
 #include "msa_internal.cuh"
@@ -24,7 +28,8 @@
 namespace msa {
 namespace {
 
-constexpr int kFwdThreads = 192;
+constexpr int kFwdThreads = 320;
+constexpr int kFwdQStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct FwdArgs {
@@ -44,21 +49,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
   constexpr int TPT = 128 / G;         // tokens per tile
+  constexpr int TPL = (TPT + 31) / 32; // tokens per producer lane
   constexpr int NCH = D / 64;          // 64-column chunks of a head row
+  constexpr int NQ = kFwdQStages;
   constexpr int kTile = 128 * D * 2;   // bytes of a 128-row, D-column bf16 tile
-  constexpr int kPTile = 128 * 128 * 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + kTile;
-  uint8_t* sQ = sV + kTile;       // [2]
-  uint8_t* sP = sQ + 2 * kTile;   // hi part of P
-  uint8_t* sPl = sP + kPTile;     // lo part of P
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sPl + kPTile);
-  // 0 kv_full | 1,2 q_full | 3,4 q_empty | 5,6 s_full | 7,8 s_empty | 9 p_full (10 unused) |
-  // 11,12 o_full | 13,14 o_empty
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint8_t* sQ = sV + kTile;  // [NQ]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + NQ * kTile);
+  // [0] kv_full | [1, 1+NQ) q_full | [1+NQ, 1+2NQ) q_empty | then per accumulator
+  // pair b in {0,1}: s_full, p_full, o_full, o_empty
+  const int B_KV = 0, B_QF = 1, B_QE = 1 + NQ, B_ACC = 1 + 2 * NQ;
+  auto b_sfull = [&](int b) { return B_ACC + 4 * b; };
+  auto b_pfull = [&](int b) { return B_ACC + 4 * b + 1; };
+  auto b_ofull = [&](int b) { return B_ACC + 4 * b + 2; };
+  auto b_oempty = [&](int b) { return B_ACC + 4 * b + 3; };
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + B_ACC + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -82,14 +91,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int slot_diag = min(j, a.K - 1);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 15; ++i) {
-      const bool four = (i == 7 || i == 8 || i == 9 || i == 10 || i == 13 || i == 14);
-      mbar_init(bar(i), four ? 4 : 1);
+    mbar_init(bar(B_KV), 1);
+    for (int s = 0; s < NQ; ++s) {
+      mbar_init(bar(B_QF + s), 1);
+      mbar_init(bar(B_QE + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(b_sfull(b)), 1);
+      mbar_init(bar(b_pfull(b)), 4);
+      mbar_init(bar(b_ofull(b)), 1);
+      mbar_init(bar(b_oempty(b)), 4);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tslot), 512);
     tmem_relinquish();
   }
@@ -97,8 +113,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(tslot);
+  // TMEM: S/P of pair b at columns [128 b, 128 b + 128), O of pair b at 256 + D b
 
-  // token of tile row-group i of tile n (T = out of range -> TMA zero fill)
+  // token and slot of row-group i of tile n (T: out of range -> TMA zero fill)
   auto tile_token = [&](int n, int i, int& t, int& slot) -> bool {
     if (n < ndiag) {
       const int qi = n * TPT + i;
@@ -118,177 +135,205 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     return t < a.T;
   };
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(0), 2 * kTile);
+      mbar_arrive_expect_tx(bar(B_KV), 2 * kTile);
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        tma_load_3d(smem_u32(sK + c * 16384), &tm_k, bar(0), 64 * c, g, kstart);
-        tma_load_3d(smem_u32(sV + c * 16384), &tm_v, bar(0), 64 * c, g, kstart);
+        tma_load_3d(smem_u32(sK + c * 16384), &tm_k, bar(B_KV), 64 * c, g, kstart);
+        tma_load_3d(smem_u32(sV + c * 16384), &tm_v, bar(B_KV), 64 * c, g, kstart);
       }
     }
-    for (int n = 0; n < ntiles; ++n) {
-      const int buf = n & 1;
-      if (n >= 2 && !wait_bar_warp(bar(3 + buf), ((n >> 1) & 1) ^ 1, abort_flag, a.status,
-                                   wait_site(kKerFwd, 3 + buf, n)))
-        break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(1 + buf), kTile);
-      __syncwarp();
-      const uint32_t qb = smem_u32(sQ + buf * kTile);
-      for (int i = lane; i < TPT; i += 32) {
-        int t, slot;
-        if (!tile_token(n, i, t, slot)) t = a.T;
+    int tok[TPL];
+    auto load_tokens = [&](int n) {
 #pragma unroll
-        for (int c = 0; c < NCH; ++c)
-          tma_load_3d(qb + c * 16384 + i * G * 128, &tm_q, bar(1 + buf), 64 * c, g * G, t);
+      for (int u = 0; u < TPL; ++u) {
+        const int i = lane + 32 * u;
+        int t = a.T, slot;
+        if (i < TPT && !tile_token(n, i, t, slot)) t = a.T;
+        tok[u] = t;
+      }
+    };
+    if (ntiles > 0) load_tokens(0);
+    for (int n = 0; n < ntiles; ++n) {
+      const int s = n % NQ;
+      if (n >= NQ && !wait_bar_warp(bar(B_QE + s), ((n / NQ) & 1) ^ 1, abort_flag, a.status,
+                                    wait_site(kKerFwd, B_QE + s, n)))
+        break;
+      int cur[TPL];
+#pragma unroll
+      for (int u = 0; u < TPL; ++u) cur[u] = tok[u];
+      if (n + 1 < ntiles) load_tokens(n + 1);
+      if (lane == 0) mbar_arrive_expect_tx(bar(B_QF + s), kTile);
+      __syncwarp();
+      const uint32_t qb = smem_u32(sQ + s * kTile);
+#pragma unroll
+      for (int u = 0; u < TPL; ++u) {
+        const int i = lane + 32 * u;
+        if (i < TPT) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c)
+            tma_load_3d(qb + c * 16384 + i * G * 128, &tm_q, bar(B_QF + s), 64 * c, g * G, cur[u]);
+        }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------ MMA issuer ---------------------------------
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
       constexpr uint32_t idO = make_idesc_bf16(128, D, false, true);
-      bool ok = wait_bar(bar(0), 0, abort_flag, a.status, wait_site(kKerFwd, 0, 0));
+      bool ok = wait_bar(bar(B_KV), 0, abort_flag, a.status, wait_site(kKerFwd, B_KV, 0));
+      const uint32_t k0 = smem_u32(sK), v0 = smem_u32(sV);
       auto issue_s = [&](int n) -> bool {
-        const int buf = n & 1, ph = (n >> 1) & 1;
-        if (!wait_bar(bar(1 + buf), ph, abort_flag, a.status, wait_site(kKerFwd, 1 + buf, n)))
+        const int s = n % NQ, b = n & 1;
+        if (!wait_bar(bar(B_QF + s), (n / NQ) & 1, abort_flag, a.status,
+                      wait_site(kKerFwd, B_QF + s, n)))
           return false;
-        if (n >= 2 &&
-            !wait_bar(bar(7 + buf), ph ^ 1, abort_flag, a.status, wait_site(kKerFwd, 7 + buf, n)))
+        // S(n) overwrites the P of tile n-2: wait until that P V has completed
+        if (n >= 2 && !wait_bar(bar(b_ofull(b)), ((n - 2) >> 1) & 1, abort_flag, a.status,
+                                wait_site(kKerFwd, b_ofull(b), n)))
           return false;
         tc_fence_after();
-        const uint32_t q0 = smem_u32(sQ + buf * kTile), k0 = smem_u32(sK);
+        const uint32_t q0 = smem_u32(sQ + s * kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16(tbase + buf * 128, make_sdesc(q0 + off, 16, 1024, kLayoutSW128),
+          umma_bf16(tbase + 128 * b, make_sdesc(q0 + off, 16, 1024, kLayoutSW128),
                     make_sdesc(k0 + off, 16, 1024, kLayoutSW128), idS, kk > 0);
         }
-        umma_commit(bar(5 + buf));
-        umma_commit(bar(3 + buf));
+        umma_commit(bar(b_sfull(b)));
+        umma_commit(bar(B_QE + s));
         return true;
       };
       if (ok && ntiles > 0) ok = issue_s(0);
-      for (int n = 0; ok && n < ntiles; ++n) {
-        const int buf = n & 1, ph = (n >> 1) & 1;
-        if (n + 1 < ntiles && !issue_s(n + 1)) break;
-        if (!wait_bar(bar(9), n & 1, abort_flag, a.status, wait_site(kKerFwd, 9, n))) break;
-        if (n >= 2 &&
-            !wait_bar(bar(13 + buf), ph ^ 1, abort_flag, a.status, wait_site(kKerFwd, 13 + buf, n)))
+      for (int n = 1; ok && n <= ntiles; ++n) {
+        // P V for tile n-1, then S for tile n
+        const int m = n - 1, b = m & 1;
+        if (!wait_bar(bar(b_pfull(b)), (m >> 1) & 1, abort_flag, a.status,
+                      wait_site(kKerFwd, b_pfull(b), m)))
+          break;
+        if (m >= 2 && !wait_bar(bar(b_oempty(b)), ((m >> 1) & 1) ^ 1, abort_flag, a.status,
+                                wait_site(kKerFwd, b_oempty(b), m)))
           break;
         tc_fence_after();
-        const uint32_t p0 = smem_u32(sP), pl0 = smem_u32(sPl), v0 = smem_u32(sV);
+        const uint32_t pa = tbase + 128 * b;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          // keys 16kk..16kk+15: hi at column 32(kk/2) + 8(kk%2), lo 16 columns further
+          const uint32_t ph = pa + 32 * (kk >> 1) + 8 * (kk & 1);
           const uint64_t bd = make_sdesc(v0 + kk * 2048, 16384, 1024, kLayoutSW128);
-          umma_bf16(tbase + 256 + buf * D, make_sdesc(p0 + off, 16, 1024, kLayoutSW128), bd, idO,
-                    kk > 0);
-          umma_bf16(tbase + 256 + buf * D, make_sdesc(pl0 + off, 16, 1024, kLayoutSW128), bd, idO,
-                    1u);
+          umma_bf16_ts(tbase + 256 + b * D, ph, bd, idO, kk > 0);
+          umma_bf16_ts(tbase + 256 + b * D, ph + 16, bd, idO, 1u);
         }
-        umma_commit(bar(11 + buf));
+        umma_commit(bar(b_ofull(b)));
+        if (n < ntiles && !issue_s(n)) break;
       }
     }
   } else {
     // ------------------------------ softmax / epilogue --------------------------
-    const int row = warp * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // Warpgroup e takes tiles n = e, e + 2, ... through accumulator pair e.
+    // Abort-safe: a failed wait marks the warp dead; it keeps walking its tiles
+    // and arriving on its barriers without touching TMEM.
+    const int e = warp >> 2;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int ti = row / G, hl = row % G;
     const float sl2 = a.scale * kLog2e;
-    for (int n = 0; n < ntiles; ++n) {
-      const int buf = n & 1, ph = (n >> 1) & 1;
+    bool dead = false;
+    for (int n = e; n < ntiles; n += 2) {
+      const int b = e, ph = (n >> 1) & 1;
       int t, slot;
       const bool valid = tile_token(n, ti, t, slot);
       const bool diag = n < ndiag;
       const int qpos = n * TPT + ti;  // position inside the block (diagonal tiles)
-      if (!wait_bar_warp(bar(5 + buf), ph, abort_flag, a.status, wait_site(kKerFwd, 5 + buf, n)))
-        break;
+      dead = dead || !wait_bar_warp(bar(b_sfull(b)), ph, abort_flag, a.status,
+                                    wait_site(kKerFwd, b_sfull(b), n));
       tc_fence_after();
-      const uint32_t ts = tbase + lane_off + buf * 128;
-      float mx = -FLT_MAX;
+      const uint32_t ts = tbase + lane_off + 128 * b;
+      float mx = -FLT_MAX, l = 0.f;
+      if (!dead) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32f(ts + c * 32, v);
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32f(ts + c * 32, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const bool keep = !diag || (c * 32 + i <= qpos);
-          mx = keep ? fmaxf(mx, v[i]) : mx;
+          for (int i = 0; i < 32; ++i) {
+            const bool keep = !diag || (c * 32 + i <= qpos);
+            mx = keep ? fmaxf(mx, v[i]) : mx;
+          }
         }
-      }
-      const float mb = mx * sl2;
-      float l = 0.f;
+        const float mb = mx * sl2;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32f(ts + c * 32, v);
-        uint32_t pk[16], pl[16];
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32f(ts + c * 32, v);
+          uint32_t w[32];  // 16 hi words then 16 lo words (keys 32c .. 32c+31)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int k0 = c * 32 + 2 * i;
-          const float p0 = (!diag || k0 <= qpos) ? exp2f(fmaf(v[2 * i], sl2, -mb)) : 0.f;
-          const float p1 = (!diag || k0 + 1 <= qpos) ? exp2f(fmaf(v[2 * i + 1], sl2, -mb)) : 0.f;
-          l += p0 + p1;
-          pk[i] = pack_bf16(p0, p1);
-          pl[i] = pack_bf16(p0 - bf16_lo(pk[i]), p1 - bf16_hi(pk[i]));
-        }
-        // 32 keys = 64 bytes = four 16-byte chunks of the row in key-chunk c/2
-        const uint32_t cbase = (c >> 1) * 16384;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t off = cbase + sw128_offset((uint32_t)row, (uint32_t)((c & 1) * 4 + q));
-          *reinterpret_cast<uint4*>(sP + off) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          *reinterpret_cast<uint4*>(sPl + off) =
-              make_uint4(pl[4 * q], pl[4 * q + 1], pl[4 * q + 2], pl[4 * q + 3]);
-        }
-      }
-      fence_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(7 + buf));
-        mbar_arrive(bar(9));
-      }
-      if (!wait_bar_warp(bar(11 + buf), ph, abort_flag, a.status, wait_site(kKerFwd, 11 + buf, n)))
-        break;
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      const uint32_t to = tbase + lane_off + 256 + buf * D;
-      float* orow = a.o_part + (((size_t)t * a.hq + g * G + hl) * a.K + slot) * (size_t)D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float v[32];
-        tmem_ld32f(to + c * 32, v);
-        if (valid) {
-          float4* dst = reinterpret_cast<float4*>(orow + c * 32);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(v[4 * q] * inv_l, v[4 * q + 1] * inv_l, v[4 * q + 2] * inv_l,
-                                 v[4 * q + 3] * inv_l);
+          for (int i = 0; i < 16; ++i) {
+            const int k0 = c * 32 + 2 * i;
+            float p0 = ex2_approx(fmaf(v[2 * i], sl2, -mb));
+            float p1 = ex2_approx(fmaf(v[2 * i + 1], sl2, -mb));
+            if (diag) {
+              p0 = k0 <= qpos ? p0 : 0.f;
+              p1 = k0 + 1 <= qpos ? p1 : 0.f;
+            }
+            l += p0 + p1;
+            const uint32_t hi = pack_bf16(p0, p1);
+            w[i] = hi;
+            w[16 + i] = pack_bf16(p0 - bf16_lo(hi), p1 - bf16_hi(hi));
+          }
+          tmem_st32(ts + c * 32, w);
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(13 + buf));
-      if (valid)
-        a.lse_part[((size_t)t * a.hq + g * G + hl) * a.K + slot] = mx * a.scale + __logf(l);
+      if (lane == 0) mbar_arrive(bar(b_pfull(b)));
+      dead = dead || !wait_bar_warp(bar(b_ofull(b)), ph, abort_flag, a.status,
+                                    wait_site(kKerFwd, b_ofull(b), n));
+      tc_fence_after();
+      if (!dead) {
+        const float inv_l = 1.f / l;
+        const uint32_t to = tbase + lane_off + 256 + b * D;
+        float* orow = a.o_part + (((size_t)t * a.hq + g * G + hl) * a.K + slot) * (size_t)D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float v[32];
+          tmem_ld32f(to + c * 32, v);
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(orow + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(v[4 * q] * inv_l, v[4 * q + 1] * inv_l, v[4 * q + 2] * inv_l,
+                                   v[4 * q + 3] * inv_l);
+          }
+        }
+        if (valid)
+          a.lse_part[((size_t)t * a.hq + g * G + hl) * a.K + slot] = mx * a.scale + __logf(l);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(b_oempty(b)));
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
 }
 
+}  // namespace
+}  // namespace msa
+
+namespace msa {
+namespace {
+
 template <int D, int G>
 cudaError_t launch_fwd_t(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st) {
-  const size_t smem = 1024 + 4 * (128 * D * 2) + 2 * (128 * 128 * 2) + 15 * 8 + 16;
+  const size_t smem = 1024 + (2 + kFwdQStages) * (128 * D * 2) + 256;
   cudaError_t e = cudaFuncSetAttribute(k_fwd<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
