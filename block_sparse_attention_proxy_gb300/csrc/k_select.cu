@@ -33,7 +33,6 @@ struct SelCfg {
   static constexpr int kTileBytes = 128 * kRowBytes;
   static constexpr uint32_t kLayout = DP == 64 ? kLayoutSW128 : kLayoutSW64;
   static constexpr uint32_t kSBO = 8 * kRowBytes;
-  static constexpr int kSwizzleBytes = DP == 64 ? 128 : 64;
 };
 
 // a ranks ahead of b: higher score, ties to the lower block id (id = block << 8 | arg)
@@ -61,15 +60,17 @@ __device__ __forceinline__ void list_insert(float (&sc)[CAP], uint32_t (&id)[CAP
   }
 }
 
-__device__ __forceinline__ float max3(float a, float b, float c) { return fmaxf(fmaxf(a, b), c); }
-
-__device__ __forceinline__ float max32(const float (&v)[32]) {
+// Maximum of 32 scores held as raw fp32 bits (16 three-input max instructions).
+__device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
   float m[11];
 #pragma unroll
-  for (int i = 0; i < 10; ++i) m[i] = max3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
-  m[10] = fmaxf(v[30], v[31]);
-  return fmaxf(fmaxf(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5])),
-               fmaxf(max3(m[6], m[7], m[8]), fmaxf(m[9], m[10])));
+  for (int i = 0; i < 10; ++i)
+    m[i] = fmax3(__uint_as_float(r[3 * i]), __uint_as_float(r[3 * i + 1]),
+                 __uint_as_float(r[3 * i + 2]));
+  m[10] = fmaxf(__uint_as_float(r[30]), __uint_as_float(r[31]));
+  const float x = fmax3(m[0], m[1], m[2]), y = fmax3(m[3], m[4], m[5]);
+  const float z = fmax3(m[6], m[7], m[8]);
+  return fmax3(fmax3(x, y, z), m[9], m[10]);
 }
 
 struct SelArgs {
@@ -223,39 +224,47 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         tc_fence_after();
         const uint32_t tb = tbase + lane_off + acc * 128;
         const bool diag = (n == J);
-        float cm[4];
+        // The 32 scores of the chunk holding the row maximum stay in registers (first chunk
+        // on ties), so the argmax needs no second TMEM read.
+        uint32_t bv[32];
+        float best = 0.f;
+        int bc = 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32f(tb + c * 32, v);
+        for (int c2 = 0; c2 < 2; ++c2) {  // 64 columns per TMEM round trip
+          uint32_t va[32], vb[32];
+          tmem_ld32x2(tb + c2 * 64, tb + c2 * 64 + 32, va, vb);
           if (diag) {
+            const uint32_t neg = __float_as_uint(-FLT_MAX);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c * 32 + i > row) v[i] = -FLT_MAX;
-          }
-          cm[c] = max32(v);
-        }
-        const float best = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
-        const int bc = cm[0] == best ? 0 : (cm[1] == best ? 1 : (cm[2] == best ? 2 : 3));
-        const bool need = diag || better(best * ps, (uint32_t)n << 8, sc[CAP - 1], id[CAP - 1]);
-        int arg = 0;
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if (__any_sync(0xffffffffu, need && bc == c)) {
-              float v[32];
-              tmem_ld32f(tb + c * 32, v);
-              if (need && bc == c) {
-                int aa = 31;
-#pragma unroll
-                for (int i = 30; i >= 0; --i) {
-                  const bool keep = diag ? (c * 32 + i <= row) : true;
-                  aa = (keep && v[i] == best) ? i : aa;
-                }
-                arg = c * 32 + aa;
-              }
+            for (int i = 0; i < 32; ++i) {
+              if (c2 * 64 + i > row) va[i] = neg;
+              if (c2 * 64 + 32 + i > row) vb[i] = neg;
             }
           }
+          const float ma = max32(va), mb = max32(vb);
+          if (c2 == 0) {
+            const bool tb1 = mb > ma;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) bv[i] = tb1 ? vb[i] : va[i];
+            best = tb1 ? mb : ma;
+            bc = tb1 ? 1 : 0;
+          } else {
+            const bool ta = ma > best;
+            const float m2 = ta ? ma : best;
+            const bool tb1 = mb > m2;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) bv[i] = tb1 ? vb[i] : (ta ? va[i] : bv[i]);
+            best = tb1 ? mb : m2;
+            bc = tb1 ? 3 : (ta ? 2 : bc);
+          }
+        }
+        const bool need = diag || better(best * ps, (uint32_t)n << 8, sc[CAP - 1], id[CAP - 1]);
+        int arg = 0;
+        if (need) {
+          int aa = 31;
+#pragma unroll
+          for (int i = 30; i >= 0; --i) aa = (__uint_as_float(bv[i]) == best) ? i : aa;
+          arg = bc * 32 + aa;
         }
         tc_fence_before();
         __syncwarp();
