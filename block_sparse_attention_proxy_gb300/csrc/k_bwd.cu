@@ -25,8 +25,14 @@
 // contiguously in the list's order, so a tile's metadata is one bulk copy.
 //
 // Roles (320 threads): warps 0-7 epilogue (two warpgroups, each half of a
-// tile's rows), warp 8 TMA producer, warp 9 MMA issuer.  Stages of {Q, dO, q_p rows, records} are multi-buffered; the next
-// tile's S^T/dP^T products run while the epilogue stores the previous dQ.
+// tile's rows), warp 8 TMA producer, warp 9 MMA issuer.  Two tiles are in
+// flight: TMEM holds two slots of {S^T, dP^T}; after the epilogue has read a
+// slot it writes P^T (bf16) back into the slot's dP^T columns, where the dV
+// product reads it as its A operand, and the slot's S^T columns receive that
+// tile's dQ^T.  dS^T has one shared-memory buffer: a tile's first dS^T
+// store waits for the previous tile's products.  The MMA warp issues
+// S^T/dP^T of tile n+1 ahead of the dV/dK/dQ products of tile n, so the
+// epilogue of one tile runs while the tensor core works on its neighbours.
 #include <cfloat>
 
 #include "msa_internal.cuh"
@@ -34,7 +40,12 @@
 namespace msa {
 namespace {
 
-constexpr int kBwdThreads = 320;
+// Warp roles: 0-7 softmax epilogue (two warpgroups), 8-11 dQ drain, 12 TMA
+// producer, 13 MMA issuer, 14-15 idle.  Register budgets per warpgroup:
+// 2 x 128 x 176 + 128 x 96 + 128 x 64 = 65536 = 512 threads x 128 at launch.
+constexpr int kBwdThreads = 512;
+constexpr int kProducerWarp = 12, kMmaWarp = 13;
+constexpr uint32_t kRegsSoftmax = 176, kRegsDq = 96, kRegsCtl = 64;
 constexpr int kRT = 64;  // rows per tile
 constexpr float kLog2eB = 1.4426950408889634f;
 
@@ -47,12 +58,17 @@ struct BwdCfg {
   static constexpr int kQChunk = kRT * 128;       // one 64-column chunk of a Q/dO tile
   static constexpr int kQpRow = 128;              // q_p rows land at a 128-byte stride
   static constexpr int kRec = bwd_rec_bytes(G);
-  static constexpr int kStage = 2 * kQT + TPT * kQpRow + TPT * kRec;
-  static constexpr int kStageAl = (kStage + 1023) / 1024 * 1024;
-  static constexpr int kFixed = 2 * kKV + 3 * 16384;  // K, V, P^T, dS^T hi, dS^T lo
+  static constexpr int kDS = 2 * 16384;           // dS^T hi and lo, [128 keys][64 rows] bf16
+  static constexpr int kQO = 2 * kQT;             // Q/dO ring stage (freed by the MMAs)
+  static constexpr int kMeta = TPT * kQpRow + TPT * kRec;  // q_p rows + records
+  static constexpr int kMetaAl = (kMeta + 127) / 128 * 128;
+  static constexpr int kFixed = 2 * kKV + kDS;  // K, V, the dS^T buffer
   static constexpr int kBars = 256;
-  static constexpr int kNS = (1024 + kFixed + 3 * kStageAl + kBars <= 232448) ? 3 : 2;
-  static constexpr int kSmem = 1024 + kFixed + kNS * kStageAl + kBars;
+  static constexpr int kRoom = 232448 - 1024 - kFixed - kBars;
+  static constexpr int kNQ = (kRoom - 2 * kMetaAl) / kQO < 4 ? (kRoom - 2 * kMetaAl) / kQO : 4;
+  static constexpr int kNM = (kRoom - kNQ * kQO) / kMetaAl < 4 ? (kRoom - kNQ * kQO) / kMetaAl : 4;
+  static constexpr int kSmem = 1024 + kFixed + kNQ * kQO + kNM * kMetaAl + kBars;
+  static_assert(kNQ >= 2 && kNM >= 2, "at least two stages of each ring");
 };
 
 struct BwdArgs {
@@ -169,26 +185,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
           const __grid_constant__ CUtensorMap tm_qp, const BwdArgs a) {
   using C = BwdCfg<D, G, DP>;
-  constexpr int TPT = C::TPT, TPL = C::TPL, NS = C::kNS, NCH = D / 64;
+  constexpr int TPT = C::TPT, TPL = C::TPL, NQ = C::kNQ, NM = C::kNM, NCH = D / 64;
   constexpr int kQT = C::kQT, kQChunk = C::kQChunk, kRec = C::kRec;
-  constexpr uint32_t T_S = 0, T_DP = 64, T_DV = 128, T_DK = 128 + D, T_DQ = 128 + 2 * D;
+  // TMEM: slot b (b = tile parity) at columns 128b: [0, 64) S^T, later dQ^T;
+  // [64, 128) dP^T, later P^T (bf16 pairs) in the first 16 columns of each
+  // warpgroup's half.  dV and dK accumulate over the whole block.
+  constexpr uint32_t T_DV = 256, T_DK = 256 + D;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + C::kKV;
-  uint8_t* sPs = sV + C::kKV;    // P^T  [128 keys][64 rows] bf16, 128B swizzle
-  uint8_t* sdS = sPs + 16384;    // dS^T hi
-  uint8_t* sdSl = sdS + 16384;   // dS^T lo; sPs..sdS double as the fp32 dQ stage
-  uint8_t* sStage = sdSl + 16384;
-  auto stQ = [&](int s) { return sStage + s * C::kStageAl; };
+  uint8_t* sDS = sV + C::kKV;  // {dS^T hi, dS^T lo}, 128B swizzle
+  uint8_t* sQO = sDS + C::kDS;
+  uint8_t* sMeta = sQO + NQ * C::kQO;
+  auto stQ = [&](int s) { return sQO + s * C::kQO; };
   auto stO = [&](int s) { return stQ(s) + kQT; };
-  auto stP = [&](int s) { return stQ(s) + 2 * kQT; };           // q_p rows
+  auto stP = [&](int s) { return sMeta + s * C::kMetaAl; };      // q_p rows
   auto stR = [&](int s) { return stP(s) + TPT * C::kQpRow; };   // records
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + NS * C::kStageAl);
-  const int B_FULL = 0, B_FREE = NS, B_SP = 2 * NS, B_DS = 2 * NS + 1, B_DQ = 2 * NS + 2,
-            B_DQT = 2 * NS + 3, B_KV = 2 * NS + 4;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * NS + 5);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sMeta + NM * C::kMetaAl);
+  // Q/dO ring: full (TMA), free (the MMA commit of dV/dK/dQ); metadata ring:
+  // full (TMA), free (the softmax and dQ warps).  Per TMEM slot: S^T/dP^T
+  // ready, dS^T/P^T ready, dQ^T ready, slot released by the dQ warps.
+  const int B_QF = 0, B_QE = NQ, B_MF = 2 * NQ, B_ME = 2 * NQ + NM, B_SP = 2 * NQ + 2 * NM,
+            B_DS = B_SP + 2, B_DQ = B_SP + 4, B_SF = B_SP + 6, B_KV = B_SP + 8, B_END = B_SP + 9;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + B_END + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -199,19 +220,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint8_t* recg = a.rec + (size_t)it.ext * kRec;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(bar(B_FULL + s), 1);
-      mbar_init(bar(B_FREE + s), 8);
+    for (int s = 0; s < NQ; ++s) {
+      mbar_init(bar(B_QF + s), 1);
+      mbar_init(bar(B_QE + s), 1);
     }
-    mbar_init(bar(B_SP), 1);
-    mbar_init(bar(B_DS), 8);
-    mbar_init(bar(B_DQ), 1);
-    mbar_init(bar(B_DQT), 8);
+    for (int s = 0; s < NM; ++s) {
+      mbar_init(bar(B_MF + s), 1);
+      mbar_init(bar(B_ME + s), 12);  // eight softmax warps and four dQ warps
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_SP + b), 1);
+      mbar_init(bar(B_DS + b), 8);
+      mbar_init(bar(B_DQ + b), 1);
+      mbar_init(bar(B_SF + b), 4);
+    }
     mbar_init(bar(B_KV), 1);
+    mbar_init(bar(B_END), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tslot), 512);
     tmem_relinquish();
   }
@@ -220,153 +248,246 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(tslot);
 
-  if (warp == 8) {
-    // ------------------------------ TMA producer --------------------------------
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(B_KV), 2 * C::kKV);
+  if (warp >= 12) {
+    setmaxnreg_dec<kRegsCtl>();
+    if (warp == kProducerWarp) {
+      // ------------------------------ TMA producer ------------------------------
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(B_KV), 2 * C::kKV);
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        tma_load_3d(smem_u32(sK + c * 16384), &tm_k, bar(B_KV), 64 * c, g, it.kstart);
-        tma_load_3d(smem_u32(sV + c * 16384), &tm_v, bar(B_KV), 64 * c, g, it.kstart);
+        for (int c = 0; c < NCH; ++c) {
+          tma_load_3d(smem_u32(sK + c * 16384), &tm_k, bar(B_KV), 64 * c, g, it.kstart);
+          tma_load_3d(smem_u32(sV + c * 16384), &tm_v, bar(B_KV), 64 * c, g, it.kstart);
+        }
+      }
+      // tokens of the next tile are read one tile ahead (records hold them)
+      auto load_tokens = [&](int n, int (&tok)[TPL]) {
+        int x0, cnt;
+        tile_span(it, n, TPT, x0, cnt);
+#pragma unroll
+        for (int u = 0; u < TPL; ++u) {
+          const int i = lane + 32 * u;
+          tok[u] = (i < TPT && i < cnt)
+                       ? __ldg(reinterpret_cast<const int*>(recg + (size_t)(x0 + i) * kRec))
+                       : a.T;
+        }
+      };
+      int tok[TPL];
+      if (it.ntiles > 0) load_tokens(0, tok);
+      int issued = 0, missued = 0;  // tiles whose Q/dO, metadata copies were issued
+      for (int n = 0; n < it.ntiles; ++n) {
+        const int sq = n % NQ, sm = n % NM;
+        if (n >= NM && !wait_bar_warp(bar(B_ME + sm), ((n / NM) & 1) ^ 1, abort_flag, a.status,
+                                      wait_site(kKerBwd, B_ME + sm, n)))
+          break;
+        int x0, cnt;
+        tile_span(it, n, TPT, x0, cnt);
+        missued = n + 1;
+        // metadata first: it does not wait for the tensor core
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_MF + sm), TPT * DP * 2 + TPT * kRec);
+          bulk_load(smem_u32(stR(sm)), recg + (size_t)x0 * kRec, TPT * kRec, bar(B_MF + sm));
+        }
+        __syncwarp();
+        const uint32_t pb = smem_u32(stP(sm));
+#pragma unroll
+        for (int u = 0; u < TPL; ++u) {
+          const int i = lane + 32 * u;
+          if (i < TPT) tma_load_3d(pb + i * C::kQpRow, &tm_qp, bar(B_MF + sm), 0, g, tok[u]);
+        }
+        if (n >= NQ && !wait_bar_warp(bar(B_QE + sq), ((n / NQ) & 1) ^ 1, abort_flag, a.status,
+                                      wait_site(kKerBwd, B_QE + sq, n)))
+          break;
+        issued = n + 1;
+        if (lane == 0) mbar_arrive_expect_tx(bar(B_QF + sq), 2 * kQT);
+        __syncwarp();
+        const uint32_t qb = smem_u32(stQ(sq)), ob = smem_u32(stO(sq));
+#pragma unroll
+        for (int u = 0; u < TPL; ++u) {
+          const int i = lane + 32 * u;
+          if (i < TPT) {
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+              tma_load_3d(qb + c * kQChunk + i * G * 128, &tm_q, bar(B_QF + sq), 64 * c, g * G,
+                          tok[u]);
+              tma_load_3d(ob + c * kQChunk + i * G * 128, &tm_do, bar(B_QF + sq), 64 * c, g * G,
+                          tok[u]);
+            }
+          }
+        }
+        if (n + 1 < it.ntiles) load_tokens(n + 1, tok);
+      }
+      // Let this CTA's own copies land before it exits (they have, unless a
+      // wait above gave up).
+      if (lane == 0) {
+        drain_bar(bar(B_KV), 0);
+        for (int n = missued > NM ? missued - NM : 0; n < missued; ++n)
+          drain_bar(bar(B_MF + n % NM), (n / NM) & 1);
+        for (int n = issued > NQ ? issued - NQ : 0; n < issued; ++n)
+          drain_bar(bar(B_QF + n % NQ), (n / NQ) & 1);
+      }
+    } else if (warp == kMmaWarp) {
+      // ------------------------------ MMA issuer -------------------------------
+      // Order: S^T/dP^T of tile n, then dV/dK/dQ^T of tile n-1.
+      if (lane == 0) {
+        constexpr uint32_t idST = make_idesc_bf16(128, kRT, false, false);
+        constexpr uint32_t idDV = make_idesc_bf16(128, D, false, true);
+        constexpr uint32_t idDQ = make_idesc_bf16(128, kRT, true, true);
+        bool ok = wait_bar(bar(B_KV), 0, abort_flag, a.status, wait_site(kKerBwd, B_KV, 0));
+        const uint32_t k0 = smem_u32(sK), v0 = smem_u32(sV);
+        for (int n = 0; ok && n <= it.ntiles; ++n) {
+          if (n < it.ntiles) {
+            const int s = n % NQ, b = n & 1;
+            if (!wait_bar(bar(B_QF + s), (n / NQ) & 1, abort_flag, a.status,
+                          wait_site(kKerBwd, B_QF + s, n)))
+              break;
+            if (n >= 2 && !wait_bar(bar(B_SF + b), ((n >> 1) - 1) & 1, abort_flag, a.status,
+                                    wait_site(kKerBwd, B_SF + b, n)))
+              break;
+            tc_fence_after();
+            const uint32_t q0 = smem_u32(stQ(s)), o0 = smem_u32(stO(s));
+            const uint32_t ts = tbase + 128u * b;
+            // S^T = K Q^T and dP^T = V dO^T   (M = 128 keys, N = 64 rows, K = D)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t kv_off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              const uint32_t q_off = (kk >> 2) * kQChunk + (kk & 3) * 32;
+              umma_bf16(ts, make_sdesc(k0 + kv_off, 16, 1024, kLayoutSW128),
+                        make_sdesc(q0 + q_off, 16, 1024, kLayoutSW128), idST, kk > 0);
+              umma_bf16(ts + 64, make_sdesc(v0 + kv_off, 16, 1024, kLayoutSW128),
+                        make_sdesc(o0 + q_off, 16, 1024, kLayoutSW128), idST, kk > 0);
+            }
+            umma_commit(bar(B_SP + b));
+          }
+          if (n >= 1) {
+            const int m = n - 1, s = m % NQ, b = m & 1;
+            if (!wait_bar(bar(B_DS + b), (m >> 1) & 1, abort_flag, a.status,
+                          wait_site(kKerBwd, B_DS + b, m)))
+              break;
+            tc_fence_after();
+            const uint32_t q0 = smem_u32(stQ(s)), o0 = smem_u32(stO(s));
+            const uint32_t ds0 = smem_u32(sDS), dl0 = ds0 + 16384;
+            const uint32_t ts = tbase + 128u * b;
+            // dV += P^T dO (P^T from TMEM), dK += (dS_hi + dS_lo)^T Q
+            // (M = 128 keys, N = D, K = 64 rows)
+#pragma unroll
+            for (int kk = 0; kk < kRT / 16; ++kk) {
+              const uint32_t acc = (m > 0 || kk > 0) ? 1u : 0u;
+              const uint64_t bdo = make_sdesc(o0 + kk * 2048, kQChunk, 1024, kLayoutSW128);
+              const uint64_t bq = make_sdesc(q0 + kk * 2048, kQChunk, 1024, kLayoutSW128);
+              umma_bf16_ts(tbase + T_DV, ts + 64 + 32 * (kk >> 1) + 8 * (kk & 1), bdo, idDV, acc);
+              umma_bf16(tbase + T_DK, make_sdesc(ds0 + kk * 32, 16, 1024, kLayoutSW128), bq,
+                        idDV, acc);
+              umma_bf16(tbase + T_DK, make_sdesc(dl0 + kk * 32, 16, 1024, kLayoutSW128), bq,
+                        idDV, 1u);
+            }
+            // dQ^T = K^T (dS_hi + dS_lo)^T into the slot's S^T columns
+            // (M = D padded to 128, N = 64 rows, K = 128 keys)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ak = make_sdesc(k0 + kk * 2048, 16384, 1024, kLayoutSW128);
+              umma_bf16(ts, ak, make_sdesc(ds0 + kk * 2048, 16384, 1024, kLayoutSW128), idDQ,
+                        kk > 0);
+              umma_bf16(ts, ak, make_sdesc(dl0 + kk * 2048, 16384, 1024, kLayoutSW128), idDQ,
+                        1u);
+            }
+            umma_commit(bar(B_DQ + b));
+            umma_commit(bar(B_QE + s));
+          }
+        }
+        // every MMA issued by this CTA completes before TMEM is released
+        umma_commit(bar(B_END));
+        drain_bar(bar(B_END), 0);
       }
     }
-    // tokens of the next tile are read one tile ahead (records hold them)
-    int tok[TPL];
-    auto load_tokens = [&](int n) {
-      int x0, cnt;
-      tile_span(it, n, TPT, x0, cnt);
+  } else if (warp >= 8) {
+    setmaxnreg_dec<kRegsDq>();
+    // ------------------------------ dQ drain -----------------------------------
+    // Warp w reads TMEM lanes 32(w-8).. (head-dim index kk) of the slot's dQ^T
+    // (64 row columns), releases the slot to the MMA warp, then writes the
+    // dq_part rows: one coalesced 128-byte store per warp and row.
+    const int kk = (warp - 8) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp - 8) * 32) << 16;
+    bool dead = false;
+    for (int m = 0; m < it.ntiles; ++m) {
+      const int s = m % NM, b = m & 1;
+      dead = dead || !wait_bar_warp(bar(B_MF + s), (m / NM) & 1, abort_flag, a.status,
+                                    wait_site(kKerBwd, B_MF + s, m));
+      dead = dead || !wait_bar_warp(bar(B_DQ + b), (m >> 1) & 1, abort_flag, a.status,
+                                    wait_site(kKerBwd, B_DQ + b, m));
+      tc_fence_after();
+      const bool act = !dead && (warp - 8) * 32 < D;  // warp-uniform
+      uint32_t va[32], vb[32];  // rows 0..31 and 32..63 of the tile
+      if (act) tmem_ld32x2(tbase + lane_off + 128u * b, tbase + lane_off + 128u * b + 32, va, vb);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SF + b));
+      if (act) {
+        int x0, cnt;
+        tile_span(it, m, TPT, x0, cnt);
+        const uint8_t* rec = stR(s);
 #pragma unroll
-      for (int u = 0; u < TPL; ++u) {
-        const int i = lane + 32 * u;
-        tok[u] = (i < TPT && i < cnt)
-                     ? __ldg(reinterpret_cast<const int*>(recg + (size_t)(x0 + i) * kRec))
-                     : a.T;
-      }
-    };
-    if (it.ntiles > 0) load_tokens(0);
-    for (int n = 0; n < it.ntiles; ++n) {
-      const int s = n % NS;
-      if (n >= NS && !wait_bar_warp(bar(B_FREE + s), ((n / NS) & 1) ^ 1, abort_flag, a.status,
-                                    wait_site(kKerBwd, B_FREE + s, n)))
-        break;
-      int cur[TPL];
+        for (int ti = 0; ti < TPT; ++ti) {
+          if (ti < cnt) {
+            const int4 hd = *reinterpret_cast<const int4*>(rec + ti * kRec);
+            if (hd.x < a.T) {
+              float* dst =
+                  a.dq_part + (((size_t)hd.x * a.hq + g * G) * a.K + hd.y) * (size_t)D + kk;
 #pragma unroll
-      for (int u = 0; u < TPL; ++u) cur[u] = tok[u];
-      if (n + 1 < it.ntiles) load_tokens(n + 1);
-      int x0, cnt;
-      tile_span(it, n, TPT, x0, cnt);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(B_FULL + s), 2 * kQT + TPT * DP * 2 + TPT * kRec);
-        bulk_load(smem_u32(stR(s)), recg + (size_t)x0 * kRec, TPT * kRec, bar(B_FULL + s));
+              for (int h = 0; h < G; ++h) {
+                const int r = ti * G + h;
+                dst[(size_t)h * a.K * D] = __uint_as_float(r < 32 ? va[r] : vb[r - 32]);
+              }
+            }
+          }
+        }
       }
       __syncwarp();
-      const uint32_t qb = smem_u32(stQ(s)), ob = smem_u32(stO(s)), pb = smem_u32(stP(s));
-#pragma unroll
-      for (int u = 0; u < TPL; ++u) {
-        const int i = lane + 32 * u;
-        if (i < TPT) {
-          const int t = cur[u];
-#pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            tma_load_3d(qb + c * kQChunk + i * G * 128, &tm_q, bar(B_FULL + s), 64 * c, g * G, t);
-            tma_load_3d(ob + c * kQChunk + i * G * 128, &tm_do, bar(B_FULL + s), 64 * c, g * G, t);
-          }
-          tma_load_3d(pb + i * C::kQpRow, &tm_qp, bar(B_FULL + s), 0, g, t);
-        }
-      }
-    }
-  } else if (warp == 9) {
-    // ------------------------------ MMA issuer ---------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idST = make_idesc_bf16(128, kRT, false, false);
-      constexpr uint32_t idDV = make_idesc_bf16(128, D, false, true);
-      constexpr uint32_t idDQ = make_idesc_bf16(128, kRT, true, true);
-      bool ok = wait_bar(bar(B_KV), 0, abort_flag, a.status, wait_site(kKerBwd, B_KV, 0));
-      const uint32_t k0 = smem_u32(sK), v0 = smem_u32(sV);
-      const uint32_t ps0 = smem_u32(sPs), ds0 = smem_u32(sdS), dl0 = smem_u32(sdSl);
-      for (int n = 0; ok && n < it.ntiles; ++n) {
-        const int s = n % NS;
-        if (!wait_bar(bar(B_FULL + s), (n / NS) & 1, abort_flag, a.status,
-                      wait_site(kKerBwd, B_FULL + s, n)))
-          break;
-        tc_fence_after();
-        const uint32_t q0 = smem_u32(stQ(s)), o0 = smem_u32(stO(s));
-        // S^T = K Q^T and dP^T = V dO^T   (M = 128 keys, N = 64 rows, K = D)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t kv_off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint32_t q_off = (kk >> 2) * kQChunk + (kk & 3) * 32;
-          umma_bf16(tbase + T_S, make_sdesc(k0 + kv_off, 16, 1024, kLayoutSW128),
-                    make_sdesc(q0 + q_off, 16, 1024, kLayoutSW128), idST, kk > 0);
-          umma_bf16(tbase + T_DP, make_sdesc(v0 + kv_off, 16, 1024, kLayoutSW128),
-                    make_sdesc(o0 + q_off, 16, 1024, kLayoutSW128), idST, kk > 0);
-        }
-        umma_commit(bar(B_SP));
-        if (!wait_bar(bar(B_DS), n & 1, abort_flag, a.status, wait_site(kKerBwd, B_DS, n))) break;
-        if (n >= 1 && !wait_bar(bar(B_DQT), (n - 1) & 1, abort_flag, a.status,
-                                wait_site(kKerBwd, B_DQT, n)))
-          break;
-        tc_fence_after();
-        // dV += P^T dO, dK += (dS_hi + dS_lo)^T Q   (M = 128 keys, N = D, K = 64 rows)
-#pragma unroll
-        for (int kk = 0; kk < kRT / 16; ++kk) {
-          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-          const uint64_t bdo = make_sdesc(o0 + kk * 2048, kQChunk, 1024, kLayoutSW128);
-          const uint64_t bq = make_sdesc(q0 + kk * 2048, kQChunk, 1024, kLayoutSW128);
-          umma_bf16(tbase + T_DV, make_sdesc(ps0 + kk * 32, 16, 1024, kLayoutSW128), bdo, idDV,
-                    acc);
-          umma_bf16(tbase + T_DK, make_sdesc(ds0 + kk * 32, 16, 1024, kLayoutSW128), bq, idDV,
-                    acc);
-          umma_bf16(tbase + T_DK, make_sdesc(dl0 + kk * 32, 16, 1024, kLayoutSW128), bq, idDV, 1u);
-        }
-        // dQ^T = K^T (dS_hi + dS_lo)^T   (M = D (padded to 128), N = 64 rows, K = 128 keys)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ak = make_sdesc(k0 + kk * 2048, 16384, 1024, kLayoutSW128);
-          umma_bf16(tbase + T_DQ, ak, make_sdesc(ds0 + kk * 2048, 16384, 1024, kLayoutSW128),
-                    idDQ, kk > 0);
-          umma_bf16(tbase + T_DQ, ak, make_sdesc(dl0 + kk * 2048, 16384, 1024, kLayoutSW128),
-                    idDQ, 1u);
-        }
-        umma_commit(bar(B_DQ));
-      }
+      if (lane == 0) mbar_arrive(bar(B_ME + s));
     }
   } else {
-    // ------------------------------ epilogue ------------------------------------
-    // Two warpgroups: warpgroup e owns tile rows 32e..32e+31 (columns of S^T,
-    // dP^T and dQ^T) for all 128 keys.  Abort-safe: a failed wait marks the
-    // warp dead; it still walks every tile and every named barrier.
+    setmaxnreg_inc<kRegsSoftmax>();
+    // ------------------------------ softmax epilogue ----------------------------
+    // Two warpgroups: warpgroup e owns tile rows 32e..32e+31 (columns of S^T
+    // and dP^T) for all 128 keys.  Abort-safe: a failed wait marks the warp
+    // dead; it still walks every tile and arrives on every barrier.
     const int e = warp >> 2;
-    const int kk = (warp & 3) * 32 + lane;  // key (S^T/dP^T/dV/dK lanes) or d index (dQ^T lanes)
+    const int kk = (warp & 3) * 32 + lane;  // key: TMEM lane of S^T, dP^T, dV, dK
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale * kLog2eB;
     const bool unit_scale = a.scale == 1.f;
-    float kp[DP];  // this warpgroup's share of the dk_p row of key kk
+    constexpr int DPH = DP / 2;
+    float kp[DPH];  // dk_p[key kk][DPH e + u]: this warpgroup's half of the row
 #pragma unroll
-    for (int u = 0; u < DP; ++u) kp[u] = 0.f;
+    for (int u = 0; u < DPH; ++u) kp[u] = 0.f;
     bool dead = false;
     for (int n = 0; n < it.ntiles; ++n) {
-      const int s = n % NS;
+      const int s = n % NM, b = n & 1;
       int x0, cnt;
       tile_span(it, n, TPT, x0, cnt);
       const bool diag = n < it.ndiag;
       const bool masked = diag || cnt < TPT;
       const uint8_t* rec = stR(s);
-      dead = dead || !wait_bar_warp(bar(B_FULL + s), (n / NS) & 1, abort_flag, a.status,
-                                    wait_site(kKerBwd, B_FULL + s, n));
-      dead = dead || !wait_bar_warp(bar(B_SP), n & 1, abort_flag, a.status,
-                                    wait_site(kKerBwd, B_SP, n));
+      uint8_t* dsh = sDS;
+      uint8_t* dsl = dsh + 16384;
+      dead = dead || !wait_bar_warp(bar(B_MF + s), (n / NM) & 1, abort_flag, a.status,
+                                    wait_site(kKerBwd, B_MF + s, n));
+      dead = dead || !wait_bar_warp(bar(B_SP + b), (n >> 1) & 1, abort_flag, a.status,
+                                    wait_site(kKerBwd, B_SP + b, n));
       tc_fence_after();
       if (!dead) {
+        const uint32_t ts = tbase + lane_off + 128u * b;
+        uint32_t pw[16];  // P^T of this warpgroup's 32 rows, bf16 pairs
 #pragma unroll
         for (int q16 = 0; q16 < 2; ++q16) {
           const int r0 = 32 * e + 16 * q16;
           uint32_t sv[16], dv[16];
-          tmem_ld16x2(tbase + lane_off + T_S + r0, tbase + lane_off + T_DP + r0, sv, dv);
-          uint32_t pp[8], dh[8], dl[8];
+          tmem_ld16x2(ts + r0, ts + 64 + r0, sv, dv);
+          uint32_t dh[8], dl[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            float pv[2], hv[2], lv[2];
+            float pv[2];
+            uint32_t hb[2], lb[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               const int r = r0 + 2 * i + u;
@@ -381,33 +502,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ds = use ? ds : 0.f;
               }
               pv[u] = p;
-              hv[u] = __bfloat162float(__float2bfloat16_rn(ds));
-              lv[u] = ds - hv[u];
+              // dS = hi + lo with hi its bf16 truncation (exact split in fp32);
+              // lo is truncated to bf16 as well: |error| < 2^-15 |dS|.
+              hb[u] = __float_as_uint(ds);
+              lb[u] = __float_as_uint(ds - __uint_as_float(hb[u] & 0xFFFF0000u));
             }
-            pp[i] = pack_bf16(pv[0], pv[1]);
-            dh[i] = pack_bf16(hv[0], hv[1]);
-            dl[i] = pack_bf16(lv[0], lv[1]);
+            pw[8 * q16 + i] = pack_bf16(pv[0], pv[1]);
+            dh[i] = pack_hi_halves(hb[0], hb[1]);
+            dl[i] = pack_hi_halves(lb[0], lb[1]);
           }
+          // the dS^T buffer was last read by the products of tile n-1, which
+          // normally completed while the first half was computed
+          if (q16 == 0 && n >= 1)
+            dead = !wait_bar_warp(bar(B_DQ + ((n - 1) & 1)), ((n - 1) >> 1) & 1, abort_flag,
+                                  a.status, wait_site(kKerBwd, B_DQ + ((n - 1) & 1), n));
+          if (dead) continue;
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const uint32_t off = sw128_offset((uint32_t)kk, (uint32_t)(r0 / 8 + q));
-            *reinterpret_cast<uint4*>(sPs + off) =
-                make_uint4(pp[4 * q], pp[4 * q + 1], pp[4 * q + 2], pp[4 * q + 3]);
-            *reinterpret_cast<uint4*>(sdS + off) =
+            *reinterpret_cast<uint4*>(dsh + off) =
                 make_uint4(dh[4 * q], dh[4 * q + 1], dh[4 * q + 2], dh[4 * q + 3]);
-            *reinterpret_cast<uint4*>(sdSl + off) =
+            *reinterpret_cast<uint4*>(dsl + off) =
                 make_uint4(dl[4 * q], dl[4 * q + 1], dl[4 * q + 2], dl[4 * q + 3]);
           }
         }
-        // fused proxy gradient: tokens (this warpgroup takes every other one)
-        // whose block argmax is this thread's key
-        for (int i = e; i < cnt; i += 2) {
+        // P^T into this warpgroup's half of the dP^T columns (already read)
+        if (!dead) tmem_st16(ts + 64 + 32 * e, pw);
+        // fused proxy gradient: tokens whose block argmax is this thread's key
+        // add g_b q_p[t] (this warpgroup's half of the dimensions)
+        for (int i = 0; i < (dead ? 0 : cnt); ++i) {
           const int4 hd = *reinterpret_cast<const int4*>(rec + i * kRec);
           if (hd.z == kk && hd.x < a.T) {
             const float gs = __int_as_float(hd.w);
-            const uint4* qrow = reinterpret_cast<const uint4*>(stP(s) + i * C::kQpRow);
+            const uint4* qrow =
+                reinterpret_cast<const uint4*>(stP(s) + i * C::kQpRow + e * DPH * 2);
 #pragma unroll
-            for (int u = 0; u < DP / 8; ++u) {
+            for (int u = 0; u < DPH / 8; ++u) {
               const uint4 w = qrow[u];
               kp[8 * u + 0] = fmaf(gs, bf16_lo(w.x), kp[8 * u + 0]);
               kp[8 * u + 1] = fmaf(gs, bf16_hi(w.x), kp[8 * u + 1]);
@@ -424,64 +554,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DS));
-      dead = dead || !wait_bar_warp(bar(B_DQ), n & 1, abort_flag, a.status,
-                                    wait_site(kKerBwd, B_DQ, n));
-      tc_fence_after();
-      // dQ^T: lane kk = head-dim index; this warpgroup's 32 row columns go to the
-      // fp32 stage [row][D] laid over sPs/sdS
-      float* stage = reinterpret_cast<float*>(sPs);
-      if (!dead) {
-        uint32_t v0[16], v1[16];
-        tmem_ld16x2(tbase + lane_off + T_DQ + 32 * e, tbase + lane_off + T_DQ + 32 * e + 16, v0,
-                    v1);
-        if (kk < D) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            stage[(32 * e + i) * D + kk] = __uint_as_float(v0[i]);
-            stage[(32 * e + 16 + i) * D + kk] = __uint_as_float(v1[i]);
-          }
-        }
+      if (lane == 0) {
+        mbar_arrive(bar(B_DS + b));
+        mbar_arrive(bar(B_ME + s));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DQT));  // the MMA may overwrite dQ^T now
-      named_bar_sync(1 + e, 128);
-      constexpr int TPR = D / 4;      // threads per row (16 bytes each)
-      constexpr int RPI = 128 / TPR;  // rows per iteration
-      if (!dead) {
-        const int tid = (warp & 3) * 32 + lane;
-#pragma unroll 4
-        for (int itn = 0; itn < 32 / RPI; ++itn) {
-          const int r = 32 * e + itn * RPI + tid / TPR, c = tid % TPR;
-          const int ti = r / G;
-          if (ti < cnt) {
-            const int4 hd = *reinterpret_cast<const int4*>(rec + ti * kRec);
-            if (hd.x < a.T) {
-              float* dst = a.dq_part +
-                           (((size_t)hd.x * a.hq + g * G + r % G) * a.K + hd.y) * (size_t)D + c * 4;
-              *reinterpret_cast<float4*>(dst) =
-                  *reinterpret_cast<const float4*>(stage + r * D + c * 4);
-            }
-          }
-        }
-      }
-      named_bar_sync(1 + e, 128);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_FREE + s));
     }
-    // dK, dV and dk_p rows of this block (lane = key), written once.  Warpgroup
-    // 1 hands its dk_p partial over through shared memory; warpgroup 0 adds it
-    // (a fixed order) and writes dk_p and dV, warpgroup 1 writes dK.  The TMEM
-    // loads are warp-collective, so every lane executes them; only the stores
-    // depend on the key being inside the document.
-    float* kbuf = reinterpret_cast<float*>(sPs);  // [DP][128]
-    named_bar_sync(3, 256);
-    if (e == 1) {
-#pragma unroll
-      for (int u = 0; u < DP; ++u) kbuf[u * 128 + kk] = kp[u];
+
+    // dK, dV and dk_p rows of this block (lane = key), written once after the
+    // last products have completed.  Warpgroup 0 writes dV, warpgroup 1 dK,
+    // each its half of dk_p.  The TMEM loads are warp-collective, so every lane
+    // executes them; only the stores depend on the key being inside the
+    // document.
+    if (it.ntiles > 0) {
+      const int m = it.ntiles - 1;
+      dead = dead || !wait_bar_warp(bar(B_DQ + (m & 1)), (m >> 1) & 1, abort_flag, a.status,
+                                    wait_site(kKerBwd, B_DQ + (m & 1), m));
     }
-    named_bar_sync(3, 256);
     tc_fence_after();
     if (!dead) {
       const bool keep = kk < it.nkeys;
@@ -499,21 +587,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
       }
-      if (keep && e == 0) {
-        float* pr = a.dk_p + krow * DP;
+      if (keep) {
+        float4* pr = reinterpret_cast<float4*>(a.dk_p + krow * DP + e * DPH);
 #pragma unroll
-        for (int q = 0; q < DP / 4; ++q)
-          reinterpret_cast<float4*>(pr)[q] =
-              make_float4(kp[4 * q] + kbuf[(4 * q) * 128 + kk],
-                          kp[4 * q + 1] + kbuf[(4 * q + 1) * 128 + kk],
-                          kp[4 * q + 2] + kbuf[(4 * q + 2) * 128 + kk],
-                          kp[4 * q + 3] + kbuf[(4 * q + 3) * 128 + kk]);
+        for (int q = 0; q < DPH / 4; ++q)
+          pr[q] = make_float4(kp[4 * q], kp[4 * q + 1], kp[4 * q + 2], kp[4 * q + 3]);
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -529,9 +613,17 @@ template <int D, int G, int DP>
 cudaError_t launch_bwd_t(const Shape& s, const CUtensorMap* m, const BwdArgs& a, cudaStream_t st) {
   using C = BwdCfg<D, G, DP>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
+  // The warpgroups' register budgets are drawn from the registers the block
+  // is launched with; a larger sum would leave setmaxnreg.inc waiting.
+  constexpr int kBudget = 2 * 128 * kRegsSoftmax + 128 * kRegsDq + 128 * kRegsCtl;
+  static_assert(kBudget <= 65536, "register budgets exceed the register file");
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, k_bwd<D, G, DP>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * kBwdThreads < kBudget) return cudaErrorInvalidConfiguration;
   k_bwd_prep<G><<<s.nb_bound * s.hkv, 128, 0, st>>>(a);
-  cudaError_t e = cudaFuncSetAttribute(k_bwd<D, G, DP>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  e = cudaFuncSetAttribute(k_bwd<D, G, DP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmem);
   if (e != cudaSuccess) return e;
   k_bwd<D, G, DP><<<s.nb_bound * s.hkv, kBwdThreads, C::kSmem, st>>>(m[0], m[1], m[2], m[3], m[4],
                                                                       a);

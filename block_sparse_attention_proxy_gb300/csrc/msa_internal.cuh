@@ -51,6 +51,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
   }
 }
+// Bounded wait that ignores the abort flag: lets this CTA's own asynchronous
+// copies or MMAs land before the CTA exits or frees TMEM.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kWaitCycles) {
+  }
+}
 // Warp-uniform form: every lane waits, the result is the AND over the warp.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
                                               volatile int* abort_flag, unsigned* status,
