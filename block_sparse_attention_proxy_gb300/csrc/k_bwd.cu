@@ -42,10 +42,10 @@ namespace {
 
 // Warp roles: 0-7 softmax epilogue (two warpgroups), 8-11 dQ drain, 12 TMA
 // producer, 13 MMA issuer, 14-15 idle.  Register budgets per warpgroup:
-// 2 x 128 x 176 + 128 x 96 + 128 x 64 = 65536 = 512 threads x 128 at launch.
+// 2 x 128 x 168 + 128 x 96 + 128 x 80 = 65536 = 512 threads x 128 at launch.
 constexpr int kBwdThreads = 512;
 constexpr int kProducerWarp = 12, kMmaWarp = 13;
-constexpr uint32_t kRegsSoftmax = 176, kRegsDq = 96, kRegsCtl = 64;
+constexpr uint32_t kRegsSoftmax = 168, kRegsDq = 96, kRegsCtl = 80;
 constexpr int kRT = 64;  // rows per tile
 constexpr float kLog2eB = 1.4426950408889634f;
 
@@ -90,7 +90,30 @@ struct BwdArgs {
   float* dv;
   float* dk_p;
   unsigned* status;
+  const uint16_t* q;   // [T][hq][d] bf16
+  const uint16_t* dO;  // [T][hq][d] bf16
 };
+
+// acc[k] += v for a warp-uniform runtime k in [0, 32): a switch keeps every
+// accumulator in a register.
+__device__ __forceinline__ void add_at32(float (&acc)[32], int k, float v) {
+  switch (k) {
+#define MSA_ADD_CASE(x) \
+  case x:               \
+    acc[x] += v;        \
+    break;
+    MSA_ADD_CASE(0) MSA_ADD_CASE(1) MSA_ADD_CASE(2) MSA_ADD_CASE(3) MSA_ADD_CASE(4)
+    MSA_ADD_CASE(5) MSA_ADD_CASE(6) MSA_ADD_CASE(7) MSA_ADD_CASE(8) MSA_ADD_CASE(9)
+    MSA_ADD_CASE(10) MSA_ADD_CASE(11) MSA_ADD_CASE(12) MSA_ADD_CASE(13) MSA_ADD_CASE(14)
+    MSA_ADD_CASE(15) MSA_ADD_CASE(16) MSA_ADD_CASE(17) MSA_ADD_CASE(18) MSA_ADD_CASE(19)
+    MSA_ADD_CASE(20) MSA_ADD_CASE(21) MSA_ADD_CASE(22) MSA_ADD_CASE(23) MSA_ADD_CASE(24)
+    MSA_ADD_CASE(25) MSA_ADD_CASE(26) MSA_ADD_CASE(27) MSA_ADD_CASE(28) MSA_ADD_CASE(29)
+    MSA_ADD_CASE(30) MSA_ADD_CASE(31)
+#undef MSA_ADD_CASE
+    default:
+      break;
+  }
+}
 
 // Work item of CTA `x`: KV group g, global block gb, the block's token range
 // and its list (diagonal tokens first, then the gathered entries).
@@ -221,7 +244,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NQ; ++s) {
-      mbar_init(bar(B_QF + s), 1);
+      mbar_init(bar(B_QF + s), 32);  // one cp.async arrival per producer lane
       mbar_init(bar(B_QE + s), 1);
     }
     for (int s = 0; s < NM; ++s) {
@@ -299,21 +322,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                       wait_site(kKerBwd, B_QE + sq, n)))
           break;
         issued = n + 1;
-        if (lane == 0) mbar_arrive_expect_tx(bar(B_QF + sq), 2 * kQT);
-        __syncwarp();
-        const uint32_t qb = smem_u32(stQ(sq)), ob = smem_u32(stO(sq));
-#pragma unroll
-        for (int u = 0; u < TPL; ++u) {
-          const int i = lane + 32 * u;
-          if (i < TPT) {
-#pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-              tma_load_3d(qb + c * kQChunk + i * G * 128, &tm_q, bar(B_QF + sq), 64 * c, g * G,
-                          tok[u]);
-              tma_load_3d(ob + c * kQChunk + i * G * 128, &tm_do, bar(B_QF + sq), 64 * c, g * G,
-                          tok[u]);
-            }
+        // Q and dO rows: 16-byte cp.async copies, lanes along a row (coalesced),
+        // written in the 128B-swizzled K-major layout the MMAs read; padding
+        // rows (token T) are zero-filled.  Each lane arrives on the stage's
+        // barrier once its copies have landed.
+        {
+          constexpr int CPR = D / 8;     // 16-byte chunks per row
+          constexpr int RPI = 32 / CPR;  // rows per warp-wide step
+          const uint32_t qb = smem_u32(stQ(sq)), ob = smem_u32(stO(sq));
+          const int c = lane % CPR;
+          const uint32_t cofs = (uint32_t)(c >> 3) * kQChunk;
+#pragma unroll 4
+          for (int k = 0; k < kRT / RPI; ++k) {
+            const int row = RPI * k + lane / CPR;
+            const int ti = row / G, h = row % G;
+            const int tu = (TPL == 1 || ti < 32) ? tok[0] : tok[TPL - 1];
+            const int t = __shfl_sync(0xffffffffu, tu, ti & 31);
+            const bool ok = t < a.T;
+            const size_t src = ((size_t)(ok ? t : 0) * a.hq + g * G + h) * D + c * 8;
+            const uint32_t dst = cofs + (uint32_t)row * 128u + ((((uint32_t)c & 7u) ^ ((uint32_t)row & 7u)) << 4);
+            cp_async16(qb + dst, a.q + src, ok ? 16u : 0u);
+            cp_async16(ob + dst, a.dO + src, ok ? 16u : 0u);
           }
+          cp_async_mbar_arrive(bar(B_QF + sq));
         }
         if (n + 1 < it.ntiles) load_tokens(n + 1, tok);
       }
@@ -344,6 +375,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (n >= 2 && !wait_bar(bar(B_SF + b), ((n >> 1) - 1) & 1, abort_flag, a.status,
                                     wait_site(kKerBwd, B_SF + b, n)))
               break;
+            // the Q/dO rows were written by cp.async (generic proxy)
+            fence_async_smem();
             tc_fence_after();
             const uint32_t q0 = smem_u32(stQ(s)), o0 = smem_u32(stO(s));
             const uint32_t ts = tbase + 128u * b;
@@ -456,10 +489,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale * kLog2eB;
     const bool unit_scale = a.scale == 1.f;
+    // Proxy key gradient: lane l of warpgroup e holds dimension DPH e + l of
+    // dk_p for the warp's 32 keys (kacc[k] <-> key 32 (warp & 3) + k).
     constexpr int DPH = DP / 2;
-    float kp[DPH];  // dk_p[key kk][DPH e + u]: this warpgroup's half of the row
+    float kacc[32];
 #pragma unroll
-    for (int u = 0; u < DPH; ++u) kp[u] = 0.f;
+    for (int k = 0; k < 32; ++k) kacc[k] = 0.f;
     bool dead = false;
     for (int n = 0; n < it.ntiles; ++n) {
       const int s = n % NM, b = n & 1;
@@ -528,26 +563,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         // P^T into this warpgroup's half of the dP^T columns (already read)
         if (!dead) tmem_st16(ts + 64 + 32 * e, pw);
-        // fused proxy gradient: tokens whose block argmax is this thread's key
-        // add g_b q_p[t] (this warpgroup's half of the dimensions)
-        for (int i = 0; i < (dead ? 0 : cnt); ++i) {
-          const int4 hd = *reinterpret_cast<const int4*>(rec + i * kRec);
-          if (hd.z == kk && hd.x < a.T) {
-            const float gs = __int_as_float(hd.w);
-            const uint4* qrow =
-                reinterpret_cast<const uint4*>(stP(s) + i * C::kQpRow + e * DPH * 2);
-#pragma unroll
-            for (int u = 0; u < DPH / 8; ++u) {
-              const uint4 w = qrow[u];
-              kp[8 * u + 0] = fmaf(gs, bf16_lo(w.x), kp[8 * u + 0]);
-              kp[8 * u + 1] = fmaf(gs, bf16_hi(w.x), kp[8 * u + 1]);
-              kp[8 * u + 2] = fmaf(gs, bf16_lo(w.y), kp[8 * u + 2]);
-              kp[8 * u + 3] = fmaf(gs, bf16_hi(w.y), kp[8 * u + 3]);
-              kp[8 * u + 4] = fmaf(gs, bf16_lo(w.z), kp[8 * u + 4]);
-              kp[8 * u + 5] = fmaf(gs, bf16_hi(w.z), kp[8 * u + 5]);
-              kp[8 * u + 6] = fmaf(gs, bf16_lo(w.w), kp[8 * u + 6]);
-              kp[8 * u + 7] = fmaf(gs, bf16_hi(w.w), kp[8 * u + 7]);
+        // fused proxy gradient: every token of the tile adds g_b q_p[t] to the
+        // dk_p row of its block argmax; the warp owning that key takes it, one
+        // dimension per lane (tokens in list order, so the sum is deterministic)
+        for (int base = 0; base < (dead ? 0 : cnt); base += 32) {
+          const int i = base + lane;
+          int ai = -1;
+          float gi = 0.f;
+          if (i < cnt) {
+            const int4 hd = *reinterpret_cast<const int4*>(rec + i * kRec);
+            if (hd.x < a.T) {
+              ai = hd.z;
+              gi = __int_as_float(hd.w);
             }
+          }
+          uint32_t mine = __ballot_sync(0xffffffffu, ai >= 0 && (ai >> 5) == (warp & 3));
+          while (mine) {
+            const int j = __ffs(mine) - 1;
+            mine &= mine - 1;
+            const int aj = __shfl_sync(0xffffffffu, ai, j);
+            const float gj = __shfl_sync(0xffffffffu, gi, j);
+            const float qv =
+                lane < DPH ? __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
+                                                 stP(s) + (base + j) * C::kQpRow +
+                                                 (DPH * e + lane) * 2)
+                                             << 16)
+                           : 0.f;
+            add_at32(kacc, aj & 31, gj * qv);
           }
         }
       }
@@ -587,11 +629,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
       }
-      if (keep) {
-        float4* pr = reinterpret_cast<float4*>(a.dk_p + krow * DP + e * DPH);
+      if (lane < DPH) {
 #pragma unroll
-        for (int q = 0; q < DPH / 4; ++q)
-          pr[q] = make_float4(kp[4 * q], kp[4 * q + 1], kp[4 * q + 2], kp[4 * q + 3]);
+        for (int k = 0; k < 32; ++k) {
+          const int key = (warp & 3) * 32 + k;
+          if (key < it.nkeys)
+            a.dk_p[((size_t)(it.kstart + key) * a.hkv + g) * DP + DPH * e + lane] = kacc[k];
+        }
       }
     }
   }
@@ -659,7 +703,7 @@ cudaError_t launch_bwd(const Shape& s, const int32_t* cu_seqlens, const int32_t*
   BwdArgs a{cu_seqlens, cu_blocks, row_ptr,    ent,        rec,          lse,         dsum,
             mass,       sel_score, sel_arg,    plse,       s.ndoc,       s.T,         s.hq,
             s.hkv,      s.K,       s.nb_bound, s.softmax_scale, s.proxy_scale, s.kl_weight,
-            dq_part,    dk,        dv,         dk_p,       status};
+            dq_part,    dk,        dv,         dk_p,       status,       q,           dO};
   if (s.d == 128)
     return s.dp == 64 ? launch_bwd_g<128, 64>(s, m, a, st) : launch_bwd_g<128, 32>(s, m, a, st);
   return s.dp == 64 ? launch_bwd_g<64, 64>(s, m, a, st) : launch_bwd_g<64, 32>(s, m, a, st);
