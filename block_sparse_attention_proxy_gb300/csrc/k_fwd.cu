@@ -19,7 +19,7 @@
 // Roles (320 threads): two softmax warpgroups (warps 0-3 and 4-7) take
 // alternate tiles through two S/O accumulator pairs, so one warpgroup's
 // softmax overlaps the other's P V product and O stores; warp 8 is the TMA
-// producer (regroup entries read one tile ahead, four Q stages); warp 9 issues
+// producer (regroup entries read one tile ahead, three Q stages); warp 9 issues
 // the MMAs.
 #include <cfloat>
 
@@ -29,7 +29,11 @@ namespace msa {
 namespace {
 
 constexpr int kFwdThreads = 320;
-constexpr int kFwdQStages = 4;
+constexpr int kFwdQStages = 3;
+// Per softmax warp: a 32-row x 32-column fp32 staging tile (128B-swizzled
+// rows) and the 32 row pointers, used to turn row-per-thread O values into
+// row-contiguous 512-byte warp stores.
+constexpr int kFwdStageWarp = 4096 + 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct FwdArgs {
@@ -59,7 +63,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint8_t* sK = smem;
   uint8_t* sV = sK + kTile;
   uint8_t* sQ = sV + kTile;  // [NQ]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + NQ * kTile);
+  uint8_t* sOst = sQ + NQ * kTile;  // [8 warps] O staging
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOst + 8 * kFwdStageWarp);
   // [0] kv_full | [1, 1+NQ) q_full | [1+NQ, 1+2NQ) q_empty | then per accumulator
   // pair b in {0,1}: s_full, p_full, o_full, o_empty
   const int B_KV = 0, B_QF = 1, B_QE = 1 + NQ, B_ACC = 1 + 2 * NQ;
@@ -293,20 +298,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                     wait_site(kKerFwd, b_ofull(b), n));
       tc_fence_after();
       if (!dead) {
+        // O row (this thread's) in 32-column chunks: TMEM -> registers (scaled
+        // by 1/l) -> swizzled staging tile -> each warp store writes 4 rows x
+        // 128 contiguous bytes.
         const float inv_l = 1.f / l;
         const uint32_t to = tbase + lane_off + 256 + b * D;
-        float* orow = a.o_part + (((size_t)t * a.hq + g * G + hl) * a.K + slot) * (size_t)D;
-#pragma unroll
+        uint8_t* stg = sOst + warp * kFwdStageWarp;
+        float** rowp = reinterpret_cast<float**>(stg + 4096);
+        rowp[lane] = valid ? a.o_part + (((size_t)t * a.hq + g * G + hl) * a.K + slot) * (size_t)D
+                           : nullptr;
+#pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float v[32];
           tmem_ld32f(to + c * 32, v);
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(orow + c * 32);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(v[4 * q] * inv_l, v[4 * q + 1] * inv_l, v[4 * q + 2] * inv_l,
-                                   v[4 * q + 3] * inv_l);
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * q] * inv_l, v[4 * q + 1] * inv_l, v[4 * q + 2] * inv_l,
+                            v[4 * q + 3] * inv_l);
+          __syncwarp();
+          const int ch = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = (lane >> 3) + 4 * i;
+            const float4 x = *reinterpret_cast<const float4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
+            float* dst = rowp[rr];
+            if (dst != nullptr) *reinterpret_cast<float4*>(dst + c * 32 + ch * 4) = x;
           }
+          __syncwarp();
         }
         if (valid)
           a.lse_part[((size_t)t * a.hq + g * G + hl) * a.K + slot] = mx * a.scale + __logf(l);
@@ -333,7 +352,7 @@ namespace {
 template <int D, int G>
 cudaError_t launch_fwd_t(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st) {
-  const size_t smem = 1024 + (2 + kFwdQStages) * (128 * D * 2) + 256;
+  const size_t smem = 1024 + (2 + kFwdQStages) * (128 * D * 2) + 8 * kFwdStageWarp + 256;
   cudaError_t e = cudaFuncSetAttribute(k_fwd<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
