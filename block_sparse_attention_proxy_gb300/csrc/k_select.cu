@@ -14,8 +14,11 @@
 // [T, blocks] matrix ever leaves the SM.
 //
 // Roles (320 threads): warps 0-3 and 4-7 are two epilogue warpgroups that take
-// key blocks alternately in pairs (TMEM accumulators 0,1 and 2,3), warp 8
-// issues TMA loads of k_p blocks into a ring, warp 9 issues tcgen05.mma.
+// key blocks alternately (three TMEM score accumulators, block n in n mod 3),
+// warp 8 issues TMA loads of k_p blocks into a ring, warp 9 issues
+// tcgen05.mma.  The q_p tile is the same for every key block: the epilogue
+// threads copy it once into TMEM, where the MMAs read it as their A operand,
+// so shared memory only feeds the k_p operand.
 #include <cfloat>
 
 #include "msa_internal.cuh"
@@ -57,6 +60,30 @@ __device__ __forceinline__ void list_insert(float (&sc)[CAP], uint32_t (&id)[CAP
     cs = take ? ts : cs;
     ci = take ? ti : ci;
     shift = take;
+  }
+}
+
+// Insert (s, nid) into the descending list sc/id when every entry already in
+// the list came from a lower block id: an equal score never displaces an
+// entry, so "ranks ahead" is a strict score comparison.  The list is sorted,
+// so the flags s > sc[i] switch from false to true once; entry i becomes
+// sc[i-1] after that point, s at it, and stays itself before it.
+template <int CAP>
+__device__ __forceinline__ void list_insert_newer(float (&sc)[CAP], uint32_t (&id)[CAP], float s,
+                                                  uint32_t nid) {
+  bool prev = false;
+  float ps = 0.f;
+  uint32_t pi = 0u;
+#pragma unroll
+  for (int i = 0; i < CAP; ++i) {
+    const bool cur = s > sc[i];
+    const float os = sc[i];
+    const uint32_t oi = id[i];
+    sc[i] = prev ? ps : (cur ? s : os);
+    id[i] = prev ? pi : (cur ? nid : oi);
+    ps = os;
+    pi = oi;
+    prev = cur;
   }
 }
 
@@ -102,14 +129,17 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   float* d_sc = reinterpret_cast<float*>(m_id + CAP * 128);                 // [128]
   uint32_t* d_id = reinterpret_cast<uint32_t*>(d_sc + 128);                 // [128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(d_id + 128);
-  // bars: 0 qfull | 1..S kvfull | S+1..2S kvempty | 2S+1..2S+4 accfull | 2S+5..2S+8 accempty
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kSelStages + 9);
+  // bars: 0 qfull | 1..S kvfull | S+1..2S kvempty | 2S+1..2S+3 accfull | 2S+4..2S+6 accempty
+  //       | 2S+7 q_p in TMEM
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kSelStages + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   const uint32_t b_qfull = smem_u32(bars);
   auto b_kvfull = [&](int s) { return smem_u32(bars + 1 + s); };
   auto b_kvempty = [&](int s) { return smem_u32(bars + 1 + kSelStages + s); };
   auto b_accfull = [&](int i) { return smem_u32(bars + 1 + 2 * kSelStages + i); };
-  auto b_accempty = [&](int i) { return smem_u32(bars + 5 + 2 * kSelStages + i); };
+  auto b_accempty = [&](int i) { return smem_u32(bars + 4 + 2 * kSelStages + i); };
+  const uint32_t b_qtmem = smem_u32(bars + 7 + 2 * kSelStages);
+  constexpr uint32_t kTQ = 384;  // TMEM columns of the q_p tile (A operand)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -133,10 +163,11 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       mbar_init(b_kvfull(s), 1);
       mbar_init(b_kvempty(s), 1);
     }
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 3; ++i) {
       mbar_init(b_accfull(i), 1);
       mbar_init(b_accempty(i), 4);
     }
+    mbar_init(b_qtmem, 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -171,23 +202,21 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     // ------------------------------ MMA issuer ---------------------------------
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc_bf16(128, 128, false, false);
-      if (wait_bar(b_qfull, 0, abort_flag, a.status, wait_site(kKerSelect, 0, 0))) {
-        const uint32_t q0 = smem_u32(sQ);
+      if (wait_bar(b_qtmem, 0, abort_flag, a.status, wait_site(kKerSelect, 0, 0))) {
         for (int n = 0; n < nblk; ++n) {
-          const int s = n % kSelStages, acc = n & 3;
+          const int s = n % kSelStages, acc = n % 3;
           if (!wait_bar(b_kvfull(s), (n / kSelStages) & 1, abort_flag, a.status,
                         wait_site(kKerSelect, 1 + s, n)))
             break;
-          if (n >= 4 && !wait_bar(b_accempty(acc), ((n >> 2) & 1) ^ 1, abort_flag, a.status,
+          if (n >= 3 && !wait_bar(b_accempty(acc), ((n / 3) & 1) ^ 1, abort_flag, a.status,
                                   wait_site(kKerSelect, 17 + acc, n)))
             break;
           tc_fence_after();
           const uint32_t k0 = smem_u32(sK + s * C::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint64_t ad = make_sdesc(q0 + kk * 32, 16, C::kSBO, C::kLayout);
             const uint64_t bd = make_sdesc(k0 + kk * 32, 16, C::kSBO, C::kLayout);
-            umma_bf16(tbase + acc * 128, ad, bd, idesc, kk > 0);
+            umma_bf16_ts(tbase + acc * 128, tbase + kTQ + 8 * kk, bd, idesc, kk > 0);
           }
           umma_commit(b_kvempty(s));
           umma_commit(b_accfull(acc));
@@ -210,13 +239,37 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     uint32_t dav = 0;
     bool handled_diag = false;
     const float ps = a.proxy_scale;
-    for (int n0 = 2 * e; n0 < nblk; n0 += 4) {
-      bool stop = false;
-      for (int u = 0; u < 2; ++u) {
-        const int n = n0 + u;
-        if (n >= nblk) break;
-        const int acc = n & 3;
-        if (!wait_bar_warp(b_accfull(acc), (n >> 2) & 1, abort_flag, a.status,
+    // q_p row of this thread (warpgroup 0; warpgroup 1 holds the same rows)
+    // from the swizzled shared tile into TMEM lane `row`, bf16 pairs per column
+    bool stop = !wait_bar_warp(b_qfull, 0, abort_flag, a.status, wait_site(kKerSelect, 20, 0));
+    if (e == 0) {
+      if (!stop) {
+        constexpr int NW = DP / 2;  // 32-bit words per row
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < NW / 4; ++c) {
+          const int sc16 = DP == 64 ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3));
+          const uint4 x = *reinterpret_cast<const uint4*>(sQ + row * C::kRowBytes + sc16 * 16);
+          w[4 * c] = x.x;
+          w[4 * c + 1] = x.y;
+          w[4 * c + 2] = x.z;
+          w[4 * c + 3] = x.w;
+        }
+#pragma unroll
+        for (int i = NW; i < 32; ++i) w[i] = 0u;
+        tmem_st32(tbase + lane_off + kTQ, w);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_qtmem);
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_qtmem);
+    }
+    for (int n = e; !stop && n < nblk; n += 2) {
+      {
+        const int acc = n % 3;
+        if (!wait_bar_warp(b_accfull(acc), (n / 3) & 1, abort_flag, a.status,
                            wait_site(kKerSelect, 13 + acc, n))) {
           stop = true;
           break;
@@ -258,7 +311,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
             bc = tb1 ? 3 : (ta ? 2 : bc);
           }
         }
-        const bool need = diag || better(best * ps, (uint32_t)n << 8, sc[CAP - 1], id[CAP - 1]);
+        // blocks reach this warpgroup in increasing order, so ties keep the older entry
+        const bool need = diag || best * ps > sc[CAP - 1];
         int arg = 0;
         if (need) {
           int aa = 31;
@@ -274,10 +328,9 @@ __global__ void __launch_bounds__(kSelThreads, 1)
           dav = ((uint32_t)n << 8) | (uint32_t)arg;
           handled_diag = true;
         } else if (need) {
-          list_insert<CAP>(sc, id, best * ps, ((uint32_t)n << 8) | (uint32_t)arg);
+          list_insert_newer<CAP>(sc, id, best * ps, ((uint32_t)n << 8) | (uint32_t)arg);
         }
       }
-      if (stop) break;
     }
     // ---- merge warpgroup 1's list into warpgroup 0's ----
     if (handled_diag) {
