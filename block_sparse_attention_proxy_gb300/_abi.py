@@ -8,6 +8,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmsa.so")
 
 MSA_OK = 0
+MSA_FLAG_REUSE_REGROUP = 0x1  # msa_bwd: reuse the block lists msa_fwd left in the workspace
 STATUS_NAMES = {
     0: "MSA_OK",
     1: "MSA_ERR_INVALID_ARG",

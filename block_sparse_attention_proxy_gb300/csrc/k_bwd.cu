@@ -159,9 +159,10 @@ __device__ __forceinline__ void tile_span(const Item& it, int n, int TPT, int& x
 }
 
 // One record per list entry of every work item, in list order:
-//   int {t, slot, arg, g_b bits} then G x float {LSE, D}, padded to 16 bytes.
-// Entries with an out-of-range token are written with t = T (the kernel then
-// treats them as padding).
+//   int {t, slot, arg, g_b bits} then G x float {-LSE log2(e), -scale D},
+// padded to 16 bytes (the epilogue then needs one FMA for each exponent and
+// one for dP - D).  Entries with an out-of-range token are written with t = T
+// and -LSE log2(e) = -inf (the kernel then treats them as padding).
 template <int G>
 __global__ void __launch_bounds__(128) k_bwd_prep(const BwdArgs a) {
   constexpr int kRec = bwd_rec_bytes(G);
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(128) k_bwd_prep(const BwdArgs a) {
     int4 hdr = make_int4(a.T, 0, 0, 0);
     float2 rows[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) rows[h] = make_float2(__int_as_float(0x7f800000), 0.f);
+    for (int h = 0; h < G; ++h) rows[h] = make_float2(__int_as_float(0xff800000), 0.f);
     if (t >= 0 && t < a.T) {
       const size_t e = ((size_t)t * a.hkv + it.g) * a.K + slot;
       const float p = __expf(__ldg(a.sel_score + e) - __ldg(a.plse + (size_t)t * a.hkv + it.g));
@@ -190,7 +191,8 @@ __global__ void __launch_bounds__(128) k_bwd_prep(const BwdArgs a) {
       hdr = make_int4(t, slot, __ldg(a.sel_arg + e) & (kBlock - 1), __float_as_int(gs));
       const size_t r0 = (size_t)t * a.hq + it.g * G;
 #pragma unroll
-      for (int h = 0; h < G; ++h) rows[h] = make_float2(__ldg(a.lse + r0 + h), __ldg(a.dsum + r0 + h));
+      for (int h = 0; h < G; ++h)
+        rows[h] = make_float2(-__ldg(a.lse + r0 + h) * kLog2eB, -a.scale * __ldg(a.dsum + r0 + h));
     }
     uint8_t* dst = const_cast<uint8_t*>(a.rec) + (size_t)(it.ext + x) * kRec;
     *reinterpret_cast<int4*>(dst) = hdr;
@@ -488,7 +490,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int kk = (warp & 3) * 32 + lane;  // key: TMEM lane of S^T, dP^T, dV, dK
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale * kLog2eB;
-    const bool unit_scale = a.scale == 1.f;
     // Proxy key gradient: lane l of warpgroup e holds dimension DPH e + l of
     // dk_p for the warp's 32 keys (kacc[k] <-> key 32 (warp & 3) + k).
     constexpr int DPH = DP / 2;
@@ -528,9 +529,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               const int r = r0 + 2 * i + u;
               const int ti = r / G, hl = r % G;
               const float2 ld = *reinterpret_cast<const float2*>(rec + ti * kRec + 16 + 8 * hl);
-              float p = ex2_approx(fmaf(__uint_as_float(sv[2 * i + u]), sl2, -ld.x * kLog2eB));
-              float ds = p * (__uint_as_float(dv[2 * i + u]) - ld.y);
-              if (!unit_scale) ds *= a.scale;
+              // record: ld.x = -LSE log2(e), ld.y = -scale D
+              float p = ex2_approx(fmaf(__uint_as_float(sv[2 * i + u]), sl2, ld.x));
+              float ds = p * fmaf(__uint_as_float(dv[2 * i + u]), a.scale, ld.y);
               if (masked) {
                 const bool use = ti < cnt && (!diag || kk <= x0 + ti);
                 p = use ? p : 0.f;

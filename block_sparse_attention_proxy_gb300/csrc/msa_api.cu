@@ -67,7 +67,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 msa_status check_params(const msa_params* p, Shape* s) {
   if (!p) return MSA_ERR_INVALID_ARG;
-  if (p->flags != 0) return MSA_ERR_INVALID_ARG;
+  if ((p->flags & ~MSA_FLAG_REUSE_REGROUP) != 0) return MSA_ERR_INVALID_ARG;
   if (p->total_tokens < 0 || p->num_docs < 1 || p->max_seqlen < 0) return MSA_ERR_INVALID_ARG;
   if (p->total_tokens > 0 && (p->max_seqlen < 1 || p->max_seqlen > p->total_tokens))
     return MSA_ERR_INVALID_ARG;
@@ -297,9 +297,12 @@ msa_status msa_bwd(const msa_params* p, const int32_t* cu_seqlens, const uint16_
   float* dsum = reinterpret_cast<float*>(base + w.dsum);
   float* dq_part = reinterpret_cast<float*>(base + w.dq_part);
   double* kl_part = reinterpret_cast<double*>(base + w.kl_part);
-  MSA_TRY(launch_meta(s, cu_seqlens, cu_blocks, status, cs));
-  MSA_TRY(launch_regroup(s, cu_seqlens, cu_blocks, sel_idx, chunk_range, cnt, row_ptr, ent,
-                         status, cs));
+  const bool reuse = (p->flags & MSA_FLAG_REUSE_REGROUP) != 0;
+  if (!reuse) {
+    MSA_TRY(launch_meta(s, cu_seqlens, cu_blocks, status, cs));
+    MSA_TRY(launch_regroup(s, cu_seqlens, cu_blocks, sel_idx, chunk_range, cnt, row_ptr, ent,
+                           status, cs));
+  }
   MSA_TRY(launch_bwd_pre(s, o, o_res, dO, dsum, cs));
   MSA_TRY(prof_mark(3, true, cs));
   MSA_TRY(launch_bwd(s, cu_seqlens, cu_blocks, row_ptr, ent, base + w.rec, q, k, v, q_p, dO, lse,
@@ -307,7 +310,7 @@ msa_status msa_bwd(const msa_params* p, const int32_t* cu_seqlens, const uint16_
   MSA_TRY(prof_mark(3, false, cs));
   MSA_TRY(launch_bwd_reduce(s, cu_seqlens, dq_part, sel_idx, sel_score, sel_arg, plse, mass, k_p,
                             dq, dq_p, kl_part, kl_loss, cs));
-  g_launches += 10;
+  g_launches += reuse ? 5 : 10;
   return MSA_OK;
 }
 

@@ -2,14 +2,17 @@
 
 The three calls run back to back on one stream and share one caller-owned
 workspace (the largest of the three sizes): the forward's slot partials are
-dead once its merge has run, so the backward reuses the same bytes.
+dead once its merge has run, so the backward reuses the same bytes, and the
+backward reuses the block lists the forward built there
+(MSA_FLAG_REUSE_REGROUP) when nothing has touched them since.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (allocate_outputs, make_params, msa_bwd, msa_bwd_workspace_size, msa_fwd,
-               msa_fwd_workspace_size, msa_proxy_select, msa_select_workspace_size, workspace)
+from . import (MSA_FLAG_REUSE_REGROUP, MsaParams, allocate_outputs, make_params, msa_bwd,
+               msa_bwd_workspace_size, msa_fwd, msa_fwd_workspace_size, msa_proxy_select,
+               msa_select_workspace_size, workspace)
 
 
 def params_for(cu_seqlens_host, hq, hkv, d, dp, top_k, **kw):
@@ -26,12 +29,17 @@ def workspace_bytes(params) -> int:
 class MSAStep:
     """Holds outputs and workspace for repeated steps at one shape."""
 
-    def __init__(self, params, device="cuda"):
+    def __init__(self, params, device="cuda", reuse_lists=True):
         self.params = params
         self.out = allocate_outputs(params, device)
         self.ws = workspace(workspace_bytes(params), device)
+        self.reuse_lists = reuse_lists
+        self._lists = None  # (cu_seqlens pointer, stream) of the forward that built the lists
+        self._bwd_params = MsaParams.from_buffer_copy(params)
+        self._bwd_params.flags = params.flags | MSA_FLAG_REUSE_REGROUP
 
     def select(self, inp, stream=None):
+        self._lists = None  # the selection (and so the block lists) may change
         o = self.out
         msa_proxy_select(self.params, inp["cu_seqlens"], inp["q_p"], inp["k_p"], o["sel_idx"],
                          o["sel_score"], o["sel_arg"], o["plse"], o["tie"], self.ws, stream)
@@ -40,14 +48,15 @@ class MSAStep:
         o = self.out
         msa_fwd(self.params, inp["cu_seqlens"], inp["q"], inp["k"], inp["v"], o["sel_idx"], o["o"],
                 o["o_res"], o["lse"], o["mass"], self.ws, stream)
+        self._lists = (inp["cu_seqlens"].data_ptr(), stream)
 
     def backward(self, inp, stream=None):
         o = self.out
-        msa_bwd(self.params, inp["cu_seqlens"], inp["q"], inp["k"], inp["v"], inp["q_p"],
-                inp["k_p"], o["o"], o["o_res"], o["lse"], o["mass"], inp["dO"], o["sel_idx"],
-                o["sel_score"],
-                o["sel_arg"], o["plse"], o["dq"], o["dk"], o["dv"], o["dq_p"], o["dk_p"],
-                o["kl_loss"], self.ws, stream)
+        reuse = self.reuse_lists and self._lists == (inp["cu_seqlens"].data_ptr(), stream)
+        msa_bwd(self._bwd_params if reuse else self.params, inp["cu_seqlens"], inp["q"], inp["k"],
+                inp["v"], inp["q_p"], inp["k_p"], o["o"], o["o_res"], o["lse"], o["mass"],
+                inp["dO"], o["sel_idx"], o["sel_score"], o["sel_arg"], o["plse"], o["dq"],
+                o["dk"], o["dv"], o["dq_p"], o["dk_p"], o["kl_loss"], self.ws, stream)
 
     def __call__(self, inp, stream=None):
         self.select(inp, stream)

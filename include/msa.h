@@ -98,8 +98,19 @@ typedef struct msa_params {
   float softmax_scale;  /* multiplies q . k (1.0 when q is pre-scaled) */
   float proxy_scale;    /* multiplies q_p . k_p (1.0 when q_p is pre-scaled) */
   float kl_weight;      /* lambda of the proxy KL loss */
-  uint32_t flags;       /* reserved, must be 0 */
+  uint32_t flags;       /* 0 or MSA_FLAG_REUSE_REGROUP; other bits are rejected */
 } msa_params;
+
+/*
+ * msa_bwd only: the workspace passed to msa_bwd is the one the preceding
+ * msa_fwd call used, on the same stream, with the same params, cu_seqlens
+ * and sel_idx, and nothing has written to it since.  msa_bwd then reuses the
+ * block lists (queries regrouped per KV block) that msa_fwd left at the front
+ * of the workspace instead of rebuilding them (5 fewer kernel launches).  The
+ * forward and backward workspace layouts share that prefix.  The other calls
+ * ignore the flag.  If the condition does not hold, the results are undefined.
+ */
+#define MSA_FLAG_REUSE_REGROUP 0x1u
 
 typedef enum msa_status {
   MSA_OK = 0,
@@ -140,7 +151,9 @@ msa_status msa_fwd(const msa_params* params, const int32_t* cu_seqlens, const ui
  * Backward of sum(o * dO) + kl_weight * sum KL.  Inputs: the forward's inputs and
  * outputs, dO, and the selection.  Outputs (all overwritten, no accumulation):
  * dq, dk, dv, dq_p, dk_p and the scalar kl_loss.  The selection is held
- * constant (it is discrete); the target mass receives no gradient.
+ * constant (it is discrete); the target mass receives no gradient.  With
+ * MSA_FLAG_REUSE_REGROUP in params->flags the block lists msa_fwd built in the
+ * same workspace are reused (see the flag).
  */
 msa_status msa_bwd(const msa_params* params, const int32_t* cu_seqlens, const uint16_t* q,
                    const uint16_t* k, const uint16_t* v, const uint16_t* q_p, const uint16_t* k_p,

@@ -55,8 +55,11 @@ def test_workspace_sizes_and_shape_checks(m):
                 m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4, block=64),
                 m.make_params(1024, 1, 1024, 4, 3, 64, 32, 4),   # hq % hkv
                 m.make_params(1024, 1, 2048, 4, 1, 64, 32, 4),   # max_seqlen > T
-                m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4, softmax_scale=0.0)):
+                m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4, softmax_scale=0.0),
+                m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4, flags=2)):  # unknown flag bit
         assert m.msa_fwd_workspace_size(bad) == 0
+    reuse = m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4, flags=m.MSA_FLAG_REUSE_REGROUP)
+    assert m.msa_bwd_workspace_size(reuse) == m.msa_bwd_workspace_size(ok)
 
 
 def _call_fwd(m, prm, ptr_val, ws_bytes):

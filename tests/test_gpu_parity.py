@@ -111,6 +111,25 @@ def test_deterministic():
         assert torch.equal(a[n], b[n]), n
 
 
+def test_backward_reusing_forward_lists_is_identical():
+    """msa_bwd with MSA_FLAG_REUSE_REGROUP (block lists left by msa_fwd in the
+    shared workspace) returns bit-for-bit what a rebuild of the lists gives."""
+    from block_sparse_attention_proxy_gb300 import msa_get_device_status
+    from block_sparse_attention_proxy_gb300.step import MSAStep, params_for
+
+    w = synth.custom([2500, 700, 1300], 8, 2, 128, 64, 5, seed=21, structured=True)
+    dev = {k: v.cuda() for k, v in synth.make_inputs(w).items()}
+    prm = params_for(dev["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k)
+    outs = []
+    for reuse in (False, True):
+        st = MSAStep(prm, reuse_lists=reuse)
+        st(dev)
+        assert msa_get_device_status() == 0
+        outs.append({k: v.clone() for k, v in st.out.items()})
+    for n in ("dq", "dk", "dv", "dq_p", "dk_p", "kl_loss"):
+        assert torch.equal(outs[0][n], outs[1][n]), n
+
+
 def test_regroup_matches_stable_sort():
     """The CSR built inside the library lists, per (group, block), exactly the
     (token, slot) pairs whose selection chose that block off the diagonal, in
