@@ -514,6 +514,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!dead) {
         const uint32_t ts = tbase + lane_off + 128u * b;
         uint32_t pw[16];  // P^T of this warpgroup's 32 rows, bf16 pairs
+        // this warpgroup's rows start at token 32e/G of the tile; every offset
+        // below is a compile-time constant
+        const uint8_t* recw = rec + (32 * e / G) * kRec + 16;
+        const int tw0 = 32 * e / G;
 #pragma unroll
         for (int q16 = 0; q16 < 2; ++q16) {
           const int r0 = 32 * e + 16 * q16;
@@ -524,12 +528,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int i = 0; i < 8; ++i) {
             float pv[2];
             uint32_t hb[2], lb[2];
+            // rows 2i, 2i+1 of the half: record entries {-LSE log2(e), -scale D}
+            float2 ldp[2];
+            const int rl = 16 * q16 + 2 * i;
+            if (G >= 2) {  // the two rows are heads h, h+1 of one token
+              const float4 x = *reinterpret_cast<const float4*>(recw + (rl / G) * kRec + 8 * (rl % G));
+              ldp[0] = make_float2(x.x, x.y);
+              ldp[1] = make_float2(x.z, x.w);
+            } else {
+              ldp[0] = *reinterpret_cast<const float2*>(recw + rl * kRec);
+              ldp[1] = *reinterpret_cast<const float2*>(recw + (rl + 1) * kRec);
+            }
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const int r = r0 + 2 * i + u;
-              const int ti = r / G, hl = r % G;
-              const float2 ld = *reinterpret_cast<const float2*>(rec + ti * kRec + 16 + 8 * hl);
-              // record: ld.x = -LSE log2(e), ld.y = -scale D
+              const int ti = tw0 + (rl + u) / G;
+              const float2 ld = ldp[u];
               float p = ex2_approx(fmaf(__uint_as_float(sv[2 * i + u]), sl2, ld.x));
               float ds = p * fmaf(__uint_as_float(dv[2 * i + u]), a.scale, ld.y);
               if (masked) {
