@@ -48,6 +48,19 @@ struct FwdArgs {
   unsigned* status;
 };
 
+// Maximum of 32 scores held as raw fp32 bits (16 three-input max instructions).
+__device__ __forceinline__ float max32_bits(const uint32_t (&r)[32]) {
+  float m[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i)
+    m[i] = fmax3(__uint_as_float(r[3 * i]), __uint_as_float(r[3 * i + 1]),
+                 __uint_as_float(r[3 * i + 2]));
+  m[10] = fmaxf(__uint_as_float(r[30]), __uint_as_float(r[31]));
+  const float x = fmax3(m[0], m[1], m[2]), y = fmax3(m[3], m[4], m[5]);
+  const float z = fmax3(m[6], m[7], m[8]);
+  return fmax3(fmax3(x, y, z), m[9], m[10]);
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -258,17 +271,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint32_t ts = tbase + lane_off + 128 * b;
       float mx = -FLT_MAX, l = 0.f;
       if (!dead) {
+        // row maximum: 64 columns per TMEM round trip, three-input max tree
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32f(ts + c * 32, v);
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t va[32], vb[32];
+          tmem_ld32x2(ts + c2 * 64, ts + c2 * 64 + 32, va, vb);
+          if (diag) {
+            const uint32_t neg = __float_as_uint(-FLT_MAX);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const bool keep = !diag || (c * 32 + i <= qpos);
-            mx = keep ? fmaxf(mx, v[i]) : mx;
+            for (int i = 0; i < 32; ++i) {
+              if (c2 * 64 + i > qpos) va[i] = neg;
+              if (c2 * 64 + 32 + i > qpos) vb[i] = neg;
+            }
           }
+          mx = fmax3(mx, max32_bits(va), max32_bits(vb));
         }
         const float mb = mx * sl2;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: no serial add chain
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float v[32];
@@ -283,13 +302,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               p0 = k0 <= qpos ? p0 : 0.f;
               p1 = k0 + 1 <= qpos ? p1 : 0.f;
             }
-            l += p0 + p1;
+            l4[i & 3] += p0 + p1;
             const uint32_t hi = pack_bf16(p0, p1);
             w[i] = hi;
             w[16 + i] = pack_bf16(p0 - bf16_lo(hi), p1 - bf16_hi(hi));
           }
           tmem_st32(ts + c * 32, w);
         }
+        l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
       }
       tc_fence_before();
       __syncwarp();
