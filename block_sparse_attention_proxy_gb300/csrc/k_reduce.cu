@@ -41,6 +41,25 @@ __global__ void __launch_bounds__(kRedWarps * 32)
   for (int hh = 0; hh < G; ++hh) {
     const size_t row = (size_t)t * hq + g * G + hh;
     const float ls = lane < nsel ? __ldg(lse_part + row * K + lane) : -INFINITY;
+    // every slot's partial is requested before any is used
+    const float* src = o_part + row * K * (size_t)D + lane * PER;
+    float x[kMaxTopK][PER];
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s) {
+      if (s < nsel) {
+        if (PER == 4) {
+          const float4 v4 = __ldg(reinterpret_cast<const float4*>(src + (size_t)s * D));
+          x[s][0] = v4.x;
+          x[s][1] = v4.y;
+          x[s][PER > 2 ? 2 : 0] = v4.z;
+          x[s][PER > 3 ? 3 : 0] = v4.w;
+        } else {
+          const float2 v2 = __ldg(reinterpret_cast<const float2*>(src + (size_t)s * D));
+          x[s][0] = v2.x;
+          x[s][1] = v2.y;
+        }
+      }
+    }
     const float mx = warp_max(ls);
     const float se = warp_sum(lane < nsel ? __expf(ls - mx) : 0.f);
     const float LSE = mx + __logf(se);
@@ -49,19 +68,12 @@ __global__ void __launch_bounds__(kRedWarps * 32)
     float acc[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u) acc[u] = 0.f;
-    const float* src = o_part + row * K * (size_t)D + lane * PER;
-    for (int s = 0; s < nsel; ++s) {
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s) {
       const float ws = __shfl_sync(0xffffffffu, w, s);
-      if (PER == 4) {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(src + (size_t)s * D));
-        acc[0] = fmaf(ws, x.x, acc[0]);
-        acc[1] = fmaf(ws, x.y, acc[1]);
-        acc[PER > 2 ? 2 : 0] = fmaf(ws, x.z, acc[PER > 2 ? 2 : 0]);
-        acc[PER > 3 ? 3 : 0] = fmaf(ws, x.w, acc[PER > 3 ? 3 : 0]);
-      } else {
-        const float2 x = __ldg(reinterpret_cast<const float2*>(src + (size_t)s * D));
-        acc[0] = fmaf(ws, x.x, acc[0]);
-        acc[1] = fmaf(ws, x.y, acc[1]);
+      if (s < nsel) {
+#pragma unroll
+        for (int u = 0; u < PER; ++u) acc[u] = fmaf(ws, x[s][u], acc[u]);
       }
     }
     uint16_t* dst = o + row * D + lane * PER;
