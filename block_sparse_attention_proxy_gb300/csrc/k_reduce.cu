@@ -101,26 +101,39 @@ __global__ void __launch_bounds__(256) k_bwd_pre(long long rows, const uint16_t*
                                                  const uint16_t* __restrict__ o_res,
                                                  const uint16_t* __restrict__ dO,
                                                  float* __restrict__ dsum) {
-  // one warp per (token, head) row; each lane reads 8 bytes of o, o_res and dO
-  constexpr int PER = D / 32;
+  // D/8 lanes per (token, head) row, 16 bytes of o, o_res and dO per lane; a warp
+  // takes kPreIters row groups and requests all of them before summing
+  constexpr int LPR = D / 8, RPW = 32 / LPR, kPreIters = 4;
   const int lane = threadIdx.x & 31;
-  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  float s = 0.f;
-  if (PER == 4) {
-    const uint2 x = __ldg(reinterpret_cast<const uint2*>(o + r * D) + lane);
-    const uint2 e = __ldg(reinterpret_cast<const uint2*>(o_res + r * D) + lane);
-    const uint2 y = __ldg(reinterpret_cast<const uint2*>(dO + r * D) + lane);
-    s = (bf16_lo(x.x) + bf16_lo(e.x)) * bf16_lo(y.x) + (bf16_hi(x.x) + bf16_hi(e.x)) * bf16_hi(y.x) +
-        (bf16_lo(x.y) + bf16_lo(e.y)) * bf16_lo(y.y) + (bf16_hi(x.y) + bf16_hi(e.y)) * bf16_hi(y.y);
-  } else {
-    const uint32_t x = __ldg(reinterpret_cast<const unsigned int*>(o + r * D) + lane);
-    const uint32_t e = __ldg(reinterpret_cast<const unsigned int*>(o_res + r * D) + lane);
-    const uint32_t y = __ldg(reinterpret_cast<const unsigned int*>(dO + r * D) + lane);
-    s = (bf16_lo(x) + bf16_lo(e)) * bf16_lo(y) + (bf16_hi(x) + bf16_hi(e)) * bf16_hi(y);
+  const long long r0 =
+      ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * (RPW * kPreIters) + lane / LPR;
+  const int c = (lane % LPR) * 8;
+  uint4 x[kPreIters], e[kPreIters], y[kPreIters];
+#pragma unroll
+  for (int u = 0; u < kPreIters; ++u) {
+    const long long r = r0 + (long long)u * RPW;
+    x[u] = e[u] = y[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (r < rows) {
+      x[u] = __ldg(reinterpret_cast<const uint4*>(o + r * D + c));
+      e[u] = __ldg(reinterpret_cast<const uint4*>(o_res + r * D + c));
+      y[u] = __ldg(reinterpret_cast<const uint4*>(dO + r * D + c));
+    }
   }
-  s = warp_sum(s);
-  if (lane == 0) dsum[r] = s;
+#pragma unroll
+  for (int u = 0; u < kPreIters; ++u) {
+    const long long r = r0 + (long long)u * RPW;
+    const uint32_t xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+    const uint32_t es[4] = {e[u].x, e[u].y, e[u].z, e[u].w};
+    const uint32_t ys[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      s += (bf16_lo(xs[q]) + bf16_lo(es[q])) * bf16_lo(ys[q]) +
+           (bf16_hi(xs[q]) + bf16_hi(es[q])) * bf16_hi(ys[q]);
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (r < rows && lane % LPR == 0) dsum[r] = s;
+  }
 }
 
 template <int D, int DP>
@@ -255,7 +268,8 @@ cudaError_t launch_fwd_merge(const Shape& s, const int32_t* cu_seqlens, const fl
 cudaError_t launch_bwd_pre(const Shape& s, const uint16_t* o, const uint16_t* o_res,
                            const uint16_t* dO, float* dsum, cudaStream_t st) {
   const long long rows = (long long)s.T * s.hq;
-  const int blocks = (int)((rows + 7) / 8);
+  const long long per_cta = 8LL * 4 * (32 / (s.d / 8));  // 8 warps x 4 row groups x rows per group
+  const int blocks = (int)((rows + per_cta - 1) / per_cta);
   if (s.d == 128)
     k_bwd_pre<128><<<blocks, 256, 0, st>>>(rows, o, o_res, dO, dsum);
   else
