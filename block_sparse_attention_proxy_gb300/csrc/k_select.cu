@@ -13,12 +13,12 @@
 // list, its lowest-index argmax.  Neither the score tile nor the pooled
 // [T, blocks] matrix ever leaves the SM.
 //
-// Roles (320 threads): warps 0-3 and 4-7 are two epilogue warpgroups that take
-// key blocks alternately (three TMEM score accumulators, block n in n mod 3),
-// warp 8 issues TMA loads of k_p blocks into a ring, warp 9 issues
-// tcgen05.mma.  The q_p tile is the same for every key block: the epilogue
-// threads copy it once into TMEM, where the MMAs read it as their A operand,
-// so shared memory only feeds the k_p operand.
+// Roles (320 threads): warps 0-3 and 4-7 are two epilogue warpgroups, warp 8
+// issues TMA loads of k_p into a ring, warp 9 issues tcgen05.mma.  Key blocks
+// go in steps of two: one 256-row k_p box per step, one N = 256 MMA chain
+// into a 256-column TMEM accumulator, and each warpgroup takes every other
+// step with its own accumulator.  The fixed cost of a step (barrier hand-offs,
+// commits) is paid once per two blocks.
 #include <cfloat>
 
 #include "msa_internal.cuh"
@@ -26,7 +26,7 @@
 namespace msa {
 namespace {
 
-constexpr int kSelStages = 6;
+constexpr int kSelStages = 4;  // k_p ring stages, two key blocks each
 constexpr int kSelThreads = 320;
 constexpr float kTieBand = 1e-3f;
 
@@ -123,23 +123,20 @@ __global__ void __launch_bounds__(kSelThreads, 1)
                                              ~uintptr_t(1023));
   // ---- shared memory carve-up ----
   uint8_t* sQ = smem;                                   // q_p tile, 128 rows
-  uint8_t* sK = sQ + C::kTileBytes;                     // k_p ring
-  float* m_sc = reinterpret_cast<float*>(sK + kSelStages * C::kTileBytes);  // [CAP][128]
+  uint8_t* sK = sQ + C::kTileBytes;                     // k_p ring: pairs of 128-key blocks
+  float* m_sc = reinterpret_cast<float*>(sK + kSelStages * 2 * C::kTileBytes);  // [CAP][128]
   uint32_t* m_id = reinterpret_cast<uint32_t*>(m_sc + CAP * 128);           // [CAP][128]
   float* d_sc = reinterpret_cast<float*>(m_id + CAP * 128);                 // [128]
   uint32_t* d_id = reinterpret_cast<uint32_t*>(d_sc + 128);                 // [128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(d_id + 128);
-  // bars: 0 qfull | 1..S kvfull | S+1..2S kvempty | 2S+1..2S+3 accfull | 2S+4..2S+6 accempty
-  //       | 2S+7 q_p in TMEM
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kSelStages + 8);
+  // bars: 0 qfull | 1..S kvfull | S+1..2S kvempty | 2S+1..2S+2 accfull | 2S+3..2S+4 accempty
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kSelStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   const uint32_t b_qfull = smem_u32(bars);
   auto b_kvfull = [&](int s) { return smem_u32(bars + 1 + s); };
   auto b_kvempty = [&](int s) { return smem_u32(bars + 1 + kSelStages + s); };
   auto b_accfull = [&](int i) { return smem_u32(bars + 1 + 2 * kSelStages + i); };
-  auto b_accempty = [&](int i) { return smem_u32(bars + 4 + 2 * kSelStages + i); };
-  const uint32_t b_qtmem = smem_u32(bars + 7 + 2 * kSelStages);
-  constexpr uint32_t kTQ = 384;  // TMEM columns of the q_p tile (A operand)
+  auto b_accempty = [&](int i) { return smem_u32(bars + 3 + 2 * kSelStages + i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -156,6 +153,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   const int qstart = dstart + J * kBlock;
   const int nrows = min(kBlock, L - J * kBlock);
   const int nblk = J + 1;
+  const int nstep = (nblk + 1) / 2;  // steps of two key blocks (the last may hold one)
 
   if (threadIdx.x == 0) {
     mbar_init(b_qfull, 1);
@@ -163,11 +161,10 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       mbar_init(b_kvfull(s), 1);
       mbar_init(b_kvempty(s), 1);
     }
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(b_accfull(i), 1);
       mbar_init(b_accempty(i), 4);
     }
-    mbar_init(b_qtmem, 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -187,36 +184,41 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       tma_prefetch_desc(&tm_kp);
       mbar_arrive_expect_tx(b_qfull, C::kTileBytes);
       tma_load_3d(smem_u32(sQ), &tm_qp, b_qfull, 0, g, qstart);
-      for (int n = 0; n < nblk; ++n) {
-        const int s = n % kSelStages;
-        if (n >= kSelStages &&
-            !wait_bar(b_kvempty(s), ((n / kSelStages) & 1) ^ 1, abort_flag, a.status,
-                      wait_site(kKerSelect, 7 + s, n)))
+      // step m: key blocks 2m and 2m+1 as one 256-row box (rows past the
+      // diagonal block, or past T, are loaded or zero-filled and never read)
+      for (int m = 0; m < nstep; ++m) {
+        const int s = m % kSelStages;
+        if (m >= kSelStages &&
+            !wait_bar(b_kvempty(s), ((m / kSelStages) & 1) ^ 1, abort_flag, a.status,
+                      wait_site(kKerSelect, 7 + s, m)))
           break;
-        mbar_arrive_expect_tx(b_kvfull(s), C::kTileBytes);
-        tma_load_3d(smem_u32(sK + s * C::kTileBytes), &tm_kp, b_kvfull(s), 0, g,
-                    dstart + n * kBlock);
+        mbar_arrive_expect_tx(b_kvfull(s), 2 * C::kTileBytes);
+        tma_load_3d(smem_u32(sK + s * 2 * C::kTileBytes), &tm_kp, b_kvfull(s), 0, g,
+                    dstart + 2 * m * kBlock);
       }
     }
   } else if (warp == 9) {
     // ------------------------------ MMA issuer ---------------------------------
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(128, 128, false, false);
-      if (wait_bar(b_qtmem, 0, abort_flag, a.status, wait_site(kKerSelect, 0, 0))) {
-        for (int n = 0; n < nblk; ++n) {
-          const int s = n % kSelStages, acc = n % 3;
-          if (!wait_bar(b_kvfull(s), (n / kSelStages) & 1, abort_flag, a.status,
-                        wait_site(kKerSelect, 1 + s, n)))
+      constexpr uint32_t idesc = make_idesc_bf16(128, 256, false, false);
+      if (wait_bar(b_qfull, 0, abort_flag, a.status, wait_site(kKerSelect, 0, 0))) {
+        const uint32_t q0 = smem_u32(sQ);
+        for (int m = 0; m < nstep; ++m) {
+          const int s = m % kSelStages, acc = m & 1;
+          if (!wait_bar(b_kvfull(s), (m / kSelStages) & 1, abort_flag, a.status,
+                        wait_site(kKerSelect, 1 + s, m)))
             break;
-          if (n >= 3 && !wait_bar(b_accempty(acc), ((n / 3) & 1) ^ 1, abort_flag, a.status,
-                                  wait_site(kKerSelect, 17 + acc, n)))
+          if (m >= 2 && !wait_bar(b_accempty(acc), ((m >> 1) & 1) ^ 1, abort_flag, a.status,
+                                  wait_site(kKerSelect, 17 + acc, m)))
             break;
           tc_fence_after();
-          const uint32_t k0 = smem_u32(sK + s * C::kTileBytes);
+          const uint32_t k0 = smem_u32(sK + s * 2 * C::kTileBytes);
+          // scores of 128 queries x 256 keys (two blocks) into a 256-column accumulator
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) {
+            const uint64_t ad = make_sdesc(q0 + kk * 32, 16, C::kSBO, C::kLayout);
             const uint64_t bd = make_sdesc(k0 + kk * 32, 16, C::kSBO, C::kLayout);
-            umma_bf16_ts(tbase + acc * 128, tbase + kTQ + 8 * kk, bd, idesc, kk > 0);
+            umma_bf16(tbase + acc * 256, ad, bd, idesc, kk > 0);
           }
           umma_commit(b_kvempty(s));
           umma_commit(b_accfull(acc));
@@ -239,43 +241,23 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     uint32_t dav = 0;
     bool handled_diag = false;
     const float ps = a.proxy_scale;
-    // q_p row of this thread (warpgroup 0; warpgroup 1 holds the same rows)
-    // from the swizzled shared tile into TMEM lane `row`, bf16 pairs per column
-    bool stop = !wait_bar_warp(b_qfull, 0, abort_flag, a.status, wait_site(kKerSelect, 20, 0));
-    if (e == 0) {
-      if (!stop) {
-        constexpr int NW = DP / 2;  // 32-bit words per row
-        uint32_t w[32];
-#pragma unroll
-        for (int c = 0; c < NW / 4; ++c) {
-          const int sc16 = DP == 64 ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3));
-          const uint4 x = *reinterpret_cast<const uint4*>(sQ + row * C::kRowBytes + sc16 * 16);
-          w[4 * c] = x.x;
-          w[4 * c + 1] = x.y;
-          w[4 * c + 2] = x.z;
-          w[4 * c + 3] = x.w;
-        }
-#pragma unroll
-        for (int i = NW; i < 32; ++i) w[i] = 0u;
-        tmem_st32(tbase + lane_off + kTQ, w);
+    // Warpgroup e takes the steps m = e, e + 2, ... (its own 256-column
+    // accumulator e); each step holds key blocks 2m and 2m + 1.
+    bool stop = false;
+    for (int m = e; !stop && m < nstep; m += 2) {
+      const int acc = m & 1;
+      if (!wait_bar_warp(b_accfull(acc), (m >> 1) & 1, abort_flag, a.status,
+                         wait_site(kKerSelect, 13 + acc, m))) {
+        stop = true;
+        break;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_qtmem);
-    } else {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_qtmem);
-    }
-    for (int n = e; !stop && n < nblk; n += 2) {
-      {
-        const int acc = n % 3;
-        if (!wait_bar_warp(b_accfull(acc), (n / 3) & 1, abort_flag, a.status,
-                           wait_site(kKerSelect, 13 + acc, n))) {
-          stop = true;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t tb = tbase + lane_off + acc * 128;
+      tc_fence_after();
+#pragma unroll 1
+      for (int u = 0; u < 2; ++u) {
+        const int n = 2 * m + u;
+        if (n >= nblk) break;  // warp-uniform
+        const bool last = u == 1 || n + 1 >= nblk;
+        const uint32_t tb = tbase + lane_off + acc * 256 + u * 128;
         const bool diag = (n == J);
         // The 32 scores of the chunk holding the row maximum stay in registers (first chunk
         // on ties), so the argmax needs no second TMEM read.
@@ -320,9 +302,11 @@ __global__ void __launch_bounds__(kSelThreads, 1)
           for (int i = 30; i >= 0; --i) aa = (__uint_as_float(bv[i]) == best) ? i : aa;
           arg = bc * 32 + aa;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_accempty(acc));
+        if (last) {  // both blocks of the step read: release the accumulator
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_accempty(acc));
+        }
         if (diag) {
           dsv = best * ps;
           dav = ((uint32_t)n << 8) | (uint32_t)arg;
@@ -436,8 +420,8 @@ template <int DP, int CAP>
 cudaError_t launch_sel_t(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
                          const SelArgs& a, cudaStream_t st) {
   using C = SelCfg<DP>;
-  const size_t smem = 1024 + (1 + kSelStages) * C::kTileBytes + CAP * 128 * 8 + 128 * 8 +
-                      (2 * kSelStages + 9) * 8 + 16;
+  const size_t smem = 1024 + (1 + 2 * kSelStages) * C::kTileBytes + CAP * 128 * 8 + 128 * 8 +
+                      (2 * kSelStages + 5) * 8 + 16;
   cudaError_t e = cudaFuncSetAttribute(k_select<DP, CAP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -456,7 +440,7 @@ cudaError_t launch_select(const Shape& s, const int32_t* cu_seqlens, const int32
   const int sw = s.dp == 64 ? 128 : 64;
   cudaError_t e;
   if ((e = make_tmap_3d(&mq, q_p, s.dp, s.hkv, s.T, s.dp, 1, 128, sw)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&mk, k_p, s.dp, s.hkv, s.T, s.dp, 1, 128, sw)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&mk, k_p, s.dp, s.hkv, s.T, s.dp, 1, 256, sw)) != cudaSuccess) return e;
   SelArgs a{cu_seqlens, cu_blocks, s.ndoc, s.T, s.hkv, s.K, s.nb_bound, s.proxy_scale,
             sel_idx,    sel_score, sel_arg, plse,   tie,  status};
   const int cap = s.K <= 4 ? 4 : (s.K <= 8 ? 8 : 16);
