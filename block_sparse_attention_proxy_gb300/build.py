@@ -20,8 +20,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmsa.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["msa_api.cu", "k_regroup.cu", "k_select.cu", "k_fwd.cu", "k_bwd.cu", "k_reduce.cu",
-           "msa_noalloc.cu"]
+SOURCES = ["msa_api.cu", "k_regroup.cu", "k_select.cu", "k_selarg.cu", "k_fwd.cu", "k_bwd.cu",
+           "k_reduce.cu", "msa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -113,7 +113,7 @@ struct SelArgs {
   unsigned* status;
 };
 
-template <int DP, int CAP>
+template <int DP, int CAP, bool ARG>
 __global__ void __launch_bounds__(kSelThreads, 1)
     k_select(const __grid_constant__ CUtensorMap tm_qp, const __grid_constant__ CUtensorMap tm_kp,
              const SelArgs a) {
@@ -259,6 +259,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         const bool last = u == 1 || n + 1 >= nblk;
         const uint32_t tb = tbase + lane_off + acc * 256 + u * 128;
         const bool diag = (n == J);
+        // argmax bookkeeping for every block (ARG), else for the diagonal block only
+        const bool track = ARG || diag;  // warp-uniform
         // The 32 scores of the chunk holding the row maximum stay in registers (first chunk
         // on ties), so the argmax needs no second TMEM read.
         uint32_t bv[32];
@@ -280,7 +282,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
           if (c2 == 0) {
             const bool tb1 = mb > ma;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) bv[i] = tb1 ? vb[i] : va[i];
+            for (int i = 0; i < 32; ++i)
+              if (track) bv[i] = tb1 ? vb[i] : va[i];
             best = tb1 ? mb : ma;
             bc = tb1 ? 1 : 0;
           } else {
@@ -288,7 +291,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
             const float m2 = ta ? ma : best;
             const bool tb1 = mb > m2;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) bv[i] = tb1 ? vb[i] : (ta ? va[i] : bv[i]);
+            for (int i = 0; i < 32; ++i)
+              if (track) bv[i] = tb1 ? vb[i] : (ta ? va[i] : bv[i]);
             best = tb1 ? mb : m2;
             bc = tb1 ? 3 : (ta ? 2 : bc);
           }
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         // blocks reach this warpgroup in increasing order, so ties keep the older entry
         const bool need = diag || best * ps > sc[CAP - 1];
         int arg = 0;
-        if (need) {
+        if (need && track) {
           int aa = 31;
 #pragma unroll
           for (int i = 30; i >= 0; --i) aa = (__uint_as_float(bv[i]) == best) ? i : aa;
@@ -416,18 +420,25 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   }
 }
 
-template <int DP, int CAP>
+template <int DP, int CAP, bool ARG>
 cudaError_t launch_sel_t(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
                          const SelArgs& a, cudaStream_t st) {
   using C = SelCfg<DP>;
   const size_t smem = 1024 + (1 + 2 * kSelStages) * C::kTileBytes + CAP * 128 * 8 + 128 * 8 +
                       (2 * kSelStages + 5) * 8 + 16;
-  cudaError_t e = cudaFuncSetAttribute(k_select<DP, CAP>,
+  cudaError_t e = cudaFuncSetAttribute(k_select<DP, CAP, ARG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = s.nb_bound * s.hkv;
-  k_select<DP, CAP><<<grid, kSelThreads, smem, st>>>(mq, mk, a);
+  k_select<DP, CAP, ARG><<<grid, kSelThreads, smem, st>>>(mq, mk, a);
   return cudaGetLastError();
+}
+
+template <int DP, int CAP>
+cudaError_t launch_sel_a(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
+                         const SelArgs& a, bool with_arg, cudaStream_t st) {
+  return with_arg ? launch_sel_t<DP, CAP, true>(s, mq, mk, a, st)
+                  : launch_sel_t<DP, CAP, false>(s, mq, mk, a, st);
 }
 
 }  // namespace
@@ -435,7 +446,7 @@ cudaError_t launch_sel_t(const Shape& s, const CUtensorMap& mq, const CUtensorMa
 cudaError_t launch_select(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
                           const uint16_t* q_p, const uint16_t* k_p, int32_t* sel_idx,
                           float* sel_score, uint8_t* sel_arg, float* plse, uint8_t* tie,
-                          unsigned* status, cudaStream_t st) {
+                          bool with_arg, unsigned* status, cudaStream_t st) {
   CUtensorMap mq, mk;
   const int sw = s.dp == 64 ? 128 : 64;
   cudaError_t e;
@@ -445,13 +456,13 @@ cudaError_t launch_select(const Shape& s, const int32_t* cu_seqlens, const int32
             sel_idx,    sel_score, sel_arg, plse,   tie,  status};
   const int cap = s.K <= 4 ? 4 : (s.K <= 8 ? 8 : 16);
   if (s.dp == 64) {
-    if (cap == 4) return launch_sel_t<64, 4>(s, mq, mk, a, st);
-    if (cap == 8) return launch_sel_t<64, 8>(s, mq, mk, a, st);
-    return launch_sel_t<64, 16>(s, mq, mk, a, st);
+    if (cap == 4) return launch_sel_a<64, 4>(s, mq, mk, a, with_arg, st);
+    if (cap == 8) return launch_sel_a<64, 8>(s, mq, mk, a, with_arg, st);
+    return launch_sel_a<64, 16>(s, mq, mk, a, with_arg, st);
   }
-  if (cap == 4) return launch_sel_t<32, 4>(s, mq, mk, a, st);
-  if (cap == 8) return launch_sel_t<32, 8>(s, mq, mk, a, st);
-  return launch_sel_t<32, 16>(s, mq, mk, a, st);
+  if (cap == 4) return launch_sel_a<32, 4>(s, mq, mk, a, with_arg, st);
+  if (cap == 8) return launch_sel_a<32, 8>(s, mq, mk, a, with_arg, st);
+  return launch_sel_a<32, 16>(s, mq, mk, a, with_arg, st);
 }
 
 }  // namespace msa

@@ -123,7 +123,8 @@ Workspace workspace_layout(const Shape& s, WsKind kind) {
     return o;
   };
   w.cu_blocks = take((size_t)(s.ndoc + 2) * 4);  // + the well-formed flag
-  if (kind == kWsFwd || kind == kWsBwd) {
+  // the block lists (regroup) form a prefix shared by all three calls
+  {
     const size_t nbs = (size_t)s.nb_bound;
     w.chunk_range = take((size_t)2 * s.nchunks * 4);
     w.cnt = take((size_t)s.nchunks * s.hkv * nbs * 4);
@@ -216,12 +217,21 @@ msa_status msa_proxy_select(const msa_params* p, const int32_t* cu_seqlens, cons
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
   int32_t* cu_blocks = reinterpret_cast<int32_t*>(base + w.cu_blocks);
+  int32_t* chunk_range = reinterpret_cast<int32_t*>(base + w.chunk_range);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(base + w.cnt);
+  int32_t* row_ptr = reinterpret_cast<int32_t*>(base + w.row_ptr);
+  uint32_t* ent = reinterpret_cast<uint32_t*>(base + w.ent);
   MSA_TRY(launch_meta(s, cu_seqlens, cu_blocks, status, cs));
   MSA_TRY(prof_mark(1, true, cs));
+  // block maxima, selection and the diagonal block's argmax
   MSA_TRY(launch_select(s, cu_seqlens, cu_blocks, q_p, k_p, sel_idx, sel_score, sel_arg, plse,
-                        tie, status, cs));
+                        tie, /*with_arg=*/false, status, cs));
   MSA_TRY(prof_mark(1, false, cs));
-  g_launches += 2;
+  // the queries of every KV block, then the argmax of each chosen earlier block
+  MSA_TRY(launch_regroup(s, cu_seqlens, cu_blocks, sel_idx, chunk_range, cnt, row_ptr, ent,
+                         status, cs));
+  MSA_TRY(launch_sel_arg(s, cu_seqlens, cu_blocks, row_ptr, ent, q_p, k_p, sel_arg, status, cs));
+  g_launches += 7;
   return MSA_OK;
 }
 
@@ -251,15 +261,18 @@ msa_status msa_fwd(const msa_params* p, const int32_t* cu_seqlens, const uint16_
   uint32_t* ent = reinterpret_cast<uint32_t*>(base + w.ent);
   float* o_part = reinterpret_cast<float*>(base + w.o_part);
   float* lse_part = reinterpret_cast<float*>(base + w.lse_part);
-  MSA_TRY(launch_meta(s, cu_seqlens, cu_blocks, status, cs));
-  MSA_TRY(launch_regroup(s, cu_seqlens, cu_blocks, sel_idx, chunk_range, cnt, row_ptr, ent,
-                         status, cs));
+  const bool reuse = (p->flags & MSA_FLAG_REUSE_REGROUP) != 0;
+  if (!reuse) {
+    MSA_TRY(launch_meta(s, cu_seqlens, cu_blocks, status, cs));
+    MSA_TRY(launch_regroup(s, cu_seqlens, cu_blocks, sel_idx, chunk_range, cnt, row_ptr, ent,
+                           status, cs));
+  }
   MSA_TRY(prof_mark(2, true, cs));
   MSA_TRY(launch_fwd(s, cu_seqlens, cu_blocks, row_ptr, ent, q, k, v, o_part, lse_part, status,
                      cs));
   MSA_TRY(prof_mark(2, false, cs));
   MSA_TRY(launch_fwd_merge(s, cu_seqlens, o_part, lse_part, o, o_res, lse, mass, cs));
-  g_launches += 7;
+  g_launches += reuse ? 2 : 7;
   return MSA_OK;
 }
 

@@ -22,7 +22,7 @@ constexpr long long kWaitCycles = 1000000000ll;
 
 // Where a bounded wait gave up, stored above the status code in the status
 // word: kernel id (4 bits), barrier index (8 bits), tile or block index (12 bits).
-enum : uint32_t { kKerSelect = 1, kKerFwd = 2, kKerBwd = 3 };
+enum : uint32_t { kKerSelect = 1, kKerFwd = 2, kKerBwd = 3, kKerSelArg = 4 };
 __host__ __device__ constexpr uint32_t wait_site(uint32_t kernel, uint32_t bar, int n) {
   return kernel | (bar << 4) | ((uint32_t)(n < 0 ? 0 : (n > 4095 ? 4095 : n)) << 12);
 }
@@ -149,10 +149,16 @@ cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, uint64_t inner, uin
 
 cudaError_t launch_meta(const Shape& s, const int32_t* cu_seqlens, int32_t* cu_blocks,
                         unsigned* status, cudaStream_t st);
+// with_arg: the selector also finds the argmax of every kept block; without
+// it only the diagonal block's, and launch_sel_arg fills in the others.
 cudaError_t launch_select(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
                           const uint16_t* q_p, const uint16_t* k_p, int32_t* sel_idx,
                           float* sel_score, uint8_t* sel_arg, float* plse, uint8_t* tie,
-                          unsigned* status, cudaStream_t st);
+                          bool with_arg, unsigned* status, cudaStream_t st);
+cudaError_t launch_sel_arg(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
+                           const int32_t* row_ptr, const uint32_t* ent, const uint16_t* q_p,
+                           const uint16_t* k_p, uint8_t* sel_arg, unsigned* status,
+                           cudaStream_t st);
 cudaError_t launch_regroup(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
                            const int32_t* sel_idx, int32_t* chunk_range, uint32_t* cnt,
                            int32_t* row_ptr, uint32_t* ent, unsigned* status, cudaStream_t st);

@@ -72,8 +72,9 @@ extern "C" msa_status msa_proxy_select_noalloc(const msa_params* p, const int32_
   if (noalloc_scratch(&cu_blocks) != cudaSuccess) return MSA_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (launch_meta(s, cu_seqlens, cu_blocks, status, cs) != cudaSuccess) return MSA_ERR_CUDA;
+  // no workspace for the block lists: the selector finds every argmax itself
   if (launch_select(s, cu_seqlens, cu_blocks, q_p, k_p, sel_idx, sel_score, sel_arg, plse, tie,
-                    status, cs) != cudaSuccess)
+                    /*with_arg=*/true, status, cs) != cudaSuccess)
     return MSA_ERR_CUDA;
   add_launches(2);
   return MSA_OK;

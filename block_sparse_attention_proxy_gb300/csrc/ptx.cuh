@@ -92,6 +92,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
                "r"(src_bytes)
                : "memory");
 }
+// Wait until every earlier cp.async of this thread has completed.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 // Arrive on `bar` once every earlier cp.async of this thread has completed; the
 // barrier's expected arrival count includes this arrival.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {

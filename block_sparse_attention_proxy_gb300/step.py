@@ -2,9 +2,10 @@
 
 The three calls run back to back on one stream and share one caller-owned
 workspace (the largest of the three sizes): the forward's slot partials are
-dead once its merge has run, so the backward reuses the same bytes, and the
-backward reuses the block lists the forward built there
-(MSA_FLAG_REUSE_REGROUP) when nothing has touched them since.
+dead once its merge has run, so the backward reuses the same bytes.  The
+selection builds the block lists (queries per KV block) at the front of the
+workspace; the forward and backward reuse them (MSA_FLAG_REUSE_REGROUP) when
+nothing has touched them since.
 """
 from __future__ import annotations
 
@@ -34,20 +35,22 @@ class MSAStep:
         self.out = allocate_outputs(params, device)
         self.ws = workspace(workspace_bytes(params), device)
         self.reuse_lists = reuse_lists
-        self._lists = None  # (cu_seqlens pointer, stream) of the forward that built the lists
-        self._bwd_params = MsaParams.from_buffer_copy(params)
+        self._lists = None  # (cu_seqlens pointer, stream) of the call that built the lists
+        self._bwd_params = MsaParams.from_buffer_copy(params)  # params + reuse flag
         self._bwd_params.flags = params.flags | MSA_FLAG_REUSE_REGROUP
 
     def select(self, inp, stream=None):
-        self._lists = None  # the selection (and so the block lists) may change
         o = self.out
         msa_proxy_select(self.params, inp["cu_seqlens"], inp["q_p"], inp["k_p"], o["sel_idx"],
                          o["sel_score"], o["sel_arg"], o["plse"], o["tie"], self.ws, stream)
+        # the call left the block lists of this selection in the workspace
+        self._lists = (inp["cu_seqlens"].data_ptr(), stream)
 
     def forward(self, inp, stream=None):
         o = self.out
-        msa_fwd(self.params, inp["cu_seqlens"], inp["q"], inp["k"], inp["v"], o["sel_idx"], o["o"],
-                o["o_res"], o["lse"], o["mass"], self.ws, stream)
+        reuse = self.reuse_lists and self._lists == (inp["cu_seqlens"].data_ptr(), stream)
+        msa_fwd(self._bwd_params if reuse else self.params, inp["cu_seqlens"], inp["q"], inp["k"],
+                inp["v"], o["sel_idx"], o["o"], o["o_res"], o["lse"], o["mass"], self.ws, stream)
         self._lists = (inp["cu_seqlens"].data_ptr(), stream)
 
     def backward(self, inp, stream=None):

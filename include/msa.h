@@ -102,13 +102,14 @@ typedef struct msa_params {
 } msa_params;
 
 /*
- * msa_bwd only: the workspace passed to msa_bwd is the one the preceding
- * msa_fwd call used, on the same stream, with the same params, cu_seqlens
- * and sel_idx, and nothing has written to it since.  msa_bwd then reuses the
- * block lists (queries regrouped per KV block) that msa_fwd left at the front
- * of the workspace instead of rebuilding them (5 fewer kernel launches).  The
- * forward and backward workspace layouts share that prefix.  The other calls
- * ignore the flag.  If the condition does not hold, the results are undefined.
+ * msa_fwd and msa_bwd: the workspace passed to the call is the one the
+ * preceding msa_proxy_select or msa_fwd call used, on the same stream, with
+ * the same params, cu_seqlens and sel_idx, and nothing has written to it
+ * since.  The call then reuses the block lists (queries regrouped per KV
+ * block) left at the front of the workspace instead of rebuilding them (5
+ * fewer kernel launches).  All three workspace layouts share that prefix.
+ * msa_proxy_select ignores the flag.  If the condition does not hold, the
+ * results are undefined.
  */
 #define MSA_FLAG_REUSE_REGROUP 0x1u
 
@@ -131,6 +132,9 @@ size_t msa_bwd_workspace_size(const msa_params* params);
  * Proxy scoring, 128-key block max-pool and top-k block selection.
  * Inputs: cu_seqlens, q_p, k_p.  Outputs: sel_idx, sel_score, sel_arg, plse, tie.
  * The [T, T] score matrix and the [T, blocks] pooled matrix are never stored.
+ * The argmax of each chosen earlier block is found after the selection, from
+ * the block lists (queries regrouped per KV block) that the call leaves at the
+ * front of the workspace for msa_fwd (see MSA_FLAG_REUSE_REGROUP).
  */
 msa_status msa_proxy_select(const msa_params* params, const int32_t* cu_seqlens,
                             const uint16_t* q_p, const uint16_t* k_p, int32_t* sel_idx,

@@ -193,7 +193,8 @@ def test_device_check_on_malformed_inputs():
     inp = synth.make_inputs(w)
     dev = {k: v.cuda() for k, v in inp.items()}
     prm = m.make_params(1024, 2, 700, 4, 2, 64, 32, 3)
-    step = MSAStep(prm)
+    # sel_idx is edited in place below, so the block lists must be rebuilt
+    step = MSAStep(prm, reuse_lists=False)
     assert m.msa_get_device_status() == 0
     bad = dict(dev)
     bad["cu_seqlens"] = torch.tensor([0, 800, 1024], dtype=torch.int32, device="cuda")  # > max_seqlen
