@@ -151,3 +151,9 @@ def allocate_outputs(params: MsaParams, device="cuda") -> dict:
         dk_p=torch.empty(T, hkv, dp, dtype=f32, device=dev),
         kl_loss=torch.zeros(1, dtype=torch.float64, device=dev),
     )
+
+
+# autograd front end (imported last: it builds on the calls above)
+from .function import MSAFunction, last_kl_loss, msa_attention  # noqa: E402
+
+__all__ += ["MSAFunction", "msa_attention", "last_kl_loss"]
