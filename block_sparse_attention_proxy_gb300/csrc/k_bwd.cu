@@ -92,6 +92,8 @@ struct BwdArgs {
   unsigned* status;
   const uint16_t* q;   // [T][hq][d] bf16
   const uint16_t* dO;  // [T][hq][d] bf16
+  int chunk;           // query chunk (qchunk_of); >= 0: dK, dV, dk_p accumulate
+  int qcb;             // KV blocks per query chunk
 };
 
 // acc[k] += v for a warp-uniform runtime k in [0, 32): a switch keeps every
@@ -119,6 +121,8 @@ __device__ __forceinline__ void add_at32(float (&acc)[32], int k, float v) {
 // and its list (diagonal tokens first, then the gathered entries).
 struct Item {
   int g, gb, j, kstart, nkeys, lbeg, lcnt, ndiag, ntiles, slot_diag;
+  int lo;         // first list entry of this launch's query chunk, relative to lbeg
+  int t0;         // first token of the query chunk (partial rows are token - t0)
   long long ext;  // index of the item's first record
 };
 
@@ -135,15 +139,26 @@ __device__ __forceinline__ bool item_of(int x, int TPT, const BwdArgs& a, Item& 
   it.kstart = dstart + it.j * kBlock;
   it.nkeys = min(kBlock, L - it.j * kBlock);
   it.lbeg = a.row_ptr[it.g * a.nb_bound + it.gb];
-  it.lcnt = a.row_ptr[it.g * a.nb_bound + it.gb + 1] - it.lbeg;
-  it.ndiag = (it.nkeys + TPT - 1) / TPT;
+  const int lend = a.row_ptr[it.g * a.nb_bound + it.gb + 1];
+  // this launch's query chunk: the block's own queries if the block is in it,
+  // and the part of its token-sorted list that falls in [t0, t1)
+  const QChunk qc = qchunk_of(a.cu, a.cu_blocks, a.ndoc, a.T, nbt, a.chunk, a.qcb);
+  int lo = it.lbeg, hi = lend;
+  if (a.chunk >= 0) {
+    lo = lower_bound_token(a.ent, it.lbeg, lend, qc.t0);
+    hi = lower_bound_token(a.ent, lo, lend, qc.t1);
+  }
+  it.lo = lo - it.lbeg;
+  it.lcnt = hi - lo;
+  it.t0 = qc.t0;
+  it.ndiag = (it.gb >= qc.b0 && it.gb < qc.b1) ? (it.nkeys + TPT - 1) / TPT : 0;
   it.ntiles = it.ndiag + (it.lcnt + TPT - 1) / TPT;
   it.slot_diag = min(it.j, a.K - 1);
   // Records of group g follow those of groups < g (their lists plus T diagonal
   // entries each); inside the group, block gb's diagonal entries are preceded
   // by kstart diagonal entries of earlier blocks.
   it.ext = (long long)it.lbeg + (long long)it.g * a.T + it.kstart;
-  return true;
+  return it.ntiles > 0;
 }
 
 // First list entry and entry count of tile n.
@@ -153,7 +168,7 @@ __device__ __forceinline__ void tile_span(const Item& it, int n, int TPT, int& x
     cnt = min(TPT, it.nkeys - x0);
   } else {
     const int m = (n - it.ndiag) * TPT;
-    x0 = it.nkeys + m;
+    x0 = it.nkeys + it.lo + m;
     cnt = min(TPT, it.lcnt - m);
   }
 }
@@ -168,15 +183,18 @@ __global__ void __launch_bounds__(128) k_bwd_prep(const BwdArgs a) {
   constexpr int kRec = bwd_rec_bytes(G);
   Item it;
   if (!item_of(blockIdx.x, kRT / G, a, it)) return;
-  const int n_ext = it.nkeys + it.lcnt;
+  const int ndg = it.ndiag > 0 ? it.nkeys : 0;  // the block's own queries, if in the chunk
+  const int n_ext = ndg + it.lcnt;
   const float gscale = a.kl_weight * a.proxy_scale;
-  for (int x = threadIdx.x; x < n_ext; x += blockDim.x) {
-    int t, slot;
-    if (x < it.nkeys) {
+  for (int y = threadIdx.x; y < n_ext; y += blockDim.x) {
+    int t, slot, x;
+    if (y < ndg) {
+      x = y;
       t = it.kstart + x;
       slot = it.slot_diag;
     } else {
-      const uint32_t e = __ldg(a.ent + it.lbeg + (x - it.nkeys));
+      x = it.nkeys + it.lo + (y - ndg);
+      const uint32_t e = __ldg(a.ent + it.lbeg + it.lo + (y - ndg));
       t = (int)(e >> 4);
       slot = (int)(e & 15u);
     }
@@ -466,8 +484,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (ti < cnt) {
             const int4 hd = *reinterpret_cast<const int4*>(rec + ti * kRec);
             if (hd.x < a.T) {
-              float* dst =
-                  a.dq_part + (((size_t)hd.x * a.hq + g * G) * a.K + hd.y) * (size_t)D + kk;
+              float* dst = a.dq_part +
+                           (((size_t)(hd.x - it.t0) * a.hq + g * G) * a.K + hd.y) * (size_t)D + kk;
 #pragma unroll
               for (int h = 0; h < G; ++h) {
                 const int r = ti * G + h;
@@ -628,6 +646,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     tc_fence_after();
     if (!dead) {
+      // dk_p first: its 32 accumulators are dead before the TMEM reads below
+      if (lane < DPH) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int key = (warp & 3) * 32 + k;
+          if (key < it.nkeys) {
+            float* pk = a.dk_p + ((size_t)(it.kstart + key) * a.hkv + g) * DP + DPH * e + lane;
+            *pk = a.chunk >= 0 ? *pk + kacc[k] : kacc[k];
+          }
+        }
+      }
       const bool keep = kk < it.nkeys;
       const size_t krow = (size_t)(it.kstart + (keep ? kk : 0)) * a.hkv + g;
       float* outr = (e == 0 ? a.dv : a.dk) + krow * D;
@@ -637,18 +666,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         float v[32];
         tmem_ld32f(tbase + lane_off + tcol + c * 32, v);
         if (keep) {
+          float4* o4 = reinterpret_cast<float4*>(outr + c * 32);
+          if (a.chunk < 0) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(outr + c * 32)[q] =
-                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
-      }
-      if (lane < DPH) {
+            for (int q = 0; q < 8; ++q)
+              o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          } else {
+            // query chunks add up, in chunk order; one float4 at a time (the
+            // empty asm keeps the loads from being batched up front)
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int key = (warp & 3) * 32 + k;
-          if (key < it.nkeys)
-            a.dk_p[((size_t)(it.kstart + key) * a.hkv + g) * DP + DPH * e + lane] = kacc[k];
+            for (int q = 0; q < 8; ++q) {
+              const float4 y = o4[q];
+              o4[q] = make_float4(y.x + v[4 * q], y.y + v[4 * q + 1], y.z + v[4 * q + 2],
+                                  y.w + v[4 * q + 3]);
+              asm volatile("" ::: "memory");
+            }
+          }
         }
       }
     }
@@ -706,7 +739,7 @@ cudaError_t launch_bwd(const Shape& s, const int32_t* cu_seqlens, const int32_t*
                        const uint16_t* q_p, const uint16_t* dO, const float* lse,
                        const float* dsum, const float* mass, const float* sel_score,
                        const uint8_t* sel_arg, const float* plse, float* dq_part, float* dk,
-                       float* dv, float* dk_p, unsigned* status, cudaStream_t st) {
+                       float* dv, float* dk_p, int chunk, unsigned* status, cudaStream_t st) {
   CUtensorMap m[5];
   cudaError_t e;
   if ((e = make_tmap_3d(&m[0], q, s.d, s.hq, s.T, 64, s.G, 1, 128)) != cudaSuccess) return e;
@@ -717,7 +750,8 @@ cudaError_t launch_bwd(const Shape& s, const int32_t* cu_seqlens, const int32_t*
   BwdArgs a{cu_seqlens, cu_blocks, row_ptr,    ent,        rec,          lse,         dsum,
             mass,       sel_score, sel_arg,    plse,       s.ndoc,       s.T,         s.hq,
             s.hkv,      s.K,       s.nb_bound, s.softmax_scale, s.proxy_scale, s.kl_weight,
-            dq_part,    dk,        dv,         dk_p,       status,       q,           dO};
+            dq_part,    dk,        dv,         dk_p,       status,       q,           dO,
+            chunk,      s.qc_blocks};
   if (s.d == 128)
     return s.dp == 64 ? launch_bwd_g<128, 64>(s, m, a, st) : launch_bwd_g<128, 32>(s, m, a, st);
   return s.dp == 64 ? launch_bwd_g<64, 64>(s, m, a, st) : launch_bwd_g<64, 32>(s, m, a, st);

@@ -43,9 +43,11 @@ struct FwdArgs {
   const uint32_t* ent;
   int ndoc, T, hq, hkv, K, nb_bound;
   float scale;
-  float* o_part;
+  float* o_part;    // rows of the query chunk: token - t0
   float* lse_part;
   unsigned* status;
+  int chunk;        // query chunk (qchunk_of)
+  int qcb;          // KV blocks per query chunk
 };
 
 // Maximum of 32 scores held as raw fp32 bits (16 three-input max instructions).
@@ -102,11 +104,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int L = a.cu[d + 1] - dstart;
   const int kstart = dstart + j * kBlock;
   const int nkeys = min(kBlock, L - j * kBlock);
-  const int lbeg = a.row_ptr[g * a.nb_bound + gb];
-  const int lcnt = a.row_ptr[g * a.nb_bound + gb + 1] - lbeg;
-  const int ndiag = (nkeys + TPT - 1) / TPT;
+  // this launch's query chunk: the block's own queries if the block is in it,
+  // and the part of its token-sorted list that falls in [t0, t1)
+  const QChunk qc = qchunk_of(a.cu, a.cu_blocks, a.ndoc, a.T, nbt, a.chunk, a.qcb);
+  int lbeg = a.row_ptr[g * a.nb_bound + gb];
+  int lend = a.row_ptr[g * a.nb_bound + gb + 1];
+  if (a.chunk >= 0) {
+    lbeg = lower_bound_token(a.ent, lbeg, lend, qc.t0);
+    lend = lower_bound_token(a.ent, lbeg, lend, qc.t1);
+  }
+  const int lcnt = lend - lbeg;
+  const bool own = gb >= qc.b0 && gb < qc.b1;
+  const int ndiag = own ? (nkeys + TPT - 1) / TPT : 0;
   const int ntiles = ndiag + (lcnt + TPT - 1) / TPT;
+  if (ntiles == 0) return;
   const int slot_diag = min(j, a.K - 1);
+  const int t0 = qc.t0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_KV), 1);
@@ -325,7 +338,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t to = tbase + lane_off + 256 + b * D;
         uint8_t* stg = sOst + warp * kFwdStageWarp;
         float** rowp = reinterpret_cast<float**>(stg + 4096);
-        rowp[lane] = valid ? a.o_part + (((size_t)t * a.hq + g * G + hl) * a.K + slot) * (size_t)D
+        rowp[lane] = valid ? a.o_part + (((size_t)(t - t0) * a.hq + g * G + hl) * a.K + slot) * (size_t)D
                            : nullptr;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -348,7 +361,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           __syncwarp();
         }
         if (valid)
-          a.lse_part[((size_t)t * a.hq + g * G + hl) * a.K + slot] = mx * a.scale + __logf(l);
+          a.lse_part[((size_t)(t - t0) * a.hq + g * G + hl) * a.K + slot] = mx * a.scale + __logf(l);
       }
       tc_fence_before();
       __syncwarp();
@@ -396,14 +409,15 @@ cudaError_t launch_fwd_d(const Shape& s, const CUtensorMap& mq, const CUtensorMa
 cudaError_t launch_fwd(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
                        const int32_t* row_ptr, const uint32_t* ent, const uint16_t* q,
                        const uint16_t* k, const uint16_t* v, float* o_part, float* lse_part,
-                       unsigned* status, cudaStream_t st) {
+                       int chunk, unsigned* status, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   cudaError_t e;
   if ((e = make_tmap_3d(&mq, q, s.d, s.hq, s.T, 64, s.G, 1, 128)) != cudaSuccess) return e;
   if ((e = make_tmap_3d(&mk, k, s.d, s.hkv, s.T, 64, 1, 128, 128)) != cudaSuccess) return e;
   if ((e = make_tmap_3d(&mv, v, s.d, s.hkv, s.T, 64, 1, 128, 128)) != cudaSuccess) return e;
   FwdArgs a{cu_seqlens, cu_blocks, row_ptr, ent,   s.ndoc, s.T,   s.hq,
-            s.hkv,      s.K,       s.nb_bound, s.softmax_scale, o_part, lse_part, status};
+            s.hkv,      s.K,       s.nb_bound, s.softmax_scale, o_part, lse_part, status,
+            chunk,      s.qc_blocks};
   return s.d == 128 ? launch_fwd_d<128>(s, mq, mk, mv, a, st)
                     : launch_fwd_d<64>(s, mq, mk, mv, a, st);
 }

@@ -26,8 +26,9 @@ __device__ __forceinline__ int nsel_of(const int32_t* cu, int ndoc, int t, int K
 
 template <int D>
 __global__ void __launch_bounds__(kRedWarps * 32)
-    k_fwd_merge(int T, int ndoc, const int32_t* __restrict__ cu, int hkv, int G, int K,
-                const float* __restrict__ o_part, const float* __restrict__ lse_part,
+    k_fwd_merge(int T, int ndoc, const int32_t* __restrict__ cu,
+                const int32_t* __restrict__ cu_blocks, int nb_bound, int chunk, int qcb, int hkv,
+                int G, int K, const float* __restrict__ o_part, const float* __restrict__ lse_part,
                 uint16_t* __restrict__ o, uint16_t* __restrict__ o_res, float* __restrict__ lse,
                 float* __restrict__ mass) {
   constexpr int PER = D / 32;  // head-dim elements per lane
@@ -35,14 +36,23 @@ __global__ void __launch_bounds__(kRedWarps * 32)
   const long long wid = (long long)blockIdx.x * kRedWarps + (threadIdx.x >> 5);
   if (wid >= (long long)T * hkv) return;
   const int t = (int)(wid / hkv), g = (int)(wid % hkv);
+  // partial rows of this launch's query chunk are indexed by token - t0
+  int t0 = 0;
+  if (chunk >= 0) {
+    const QChunk qc =
+        qchunk_of(cu, cu_blocks, ndoc, T, min(cu_blocks[ndoc], nb_bound), chunk, qcb);
+    if (t < qc.t0 || t >= qc.t1) return;
+    t0 = qc.t0;
+  }
   const int hq = hkv * G;
   const int nsel = nsel_of(cu, ndoc, t, K);
   float macc = 0.f;
   for (int hh = 0; hh < G; ++hh) {
     const size_t row = (size_t)t * hq + g * G + hh;
-    const float ls = lane < nsel ? __ldg(lse_part + row * K + lane) : -INFINITY;
+    const size_t prow = (size_t)(t - t0) * hq + g * G + hh;
+    const float ls = lane < nsel ? __ldg(lse_part + prow * K + lane) : -INFINITY;
     // every slot's partial is requested before any is used
-    const float* src = o_part + row * K * (size_t)D + lane * PER;
+    const float* src = o_part + prow * K * (size_t)D + lane * PER;
     float x[kMaxTopK][PER];
 #pragma unroll
     for (int s = 0; s < kMaxTopK; ++s) {
@@ -138,8 +148,9 @@ __global__ void __launch_bounds__(256) k_bwd_pre(long long rows, const uint16_t*
 
 template <int D, int DP>
 __global__ void __launch_bounds__(kRedWarps * 32)
-    k_bwd_reduce(int T, int ndoc, const int32_t* __restrict__ cu, int hkv, int G, int K,
-                 float proxy_scale, float kl_weight, const float* __restrict__ dq_part,
+    k_bwd_reduce(int T, int ndoc, const int32_t* __restrict__ cu,
+                 const int32_t* __restrict__ cu_blocks, int nb_bound, int chunk, int qcb, int hkv,
+                 int G, int K, float proxy_scale, float kl_weight, const float* __restrict__ dq_part,
                  const int32_t* __restrict__ sel_idx, const float* __restrict__ sel_score,
                  const uint8_t* __restrict__ sel_arg, const float* __restrict__ plse,
                  const float* __restrict__ mass, const uint16_t* __restrict__ k_p,
@@ -150,8 +161,17 @@ __global__ void __launch_bounds__(kRedWarps * 32)
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const long long wid = (long long)blockIdx.x * kRedWarps + w;
   double kl_w = 0.0;
-  if (wid < (long long)T * hkv) {
-    const int t = (int)(wid / hkv), g = (int)(wid % hkv);
+  // partial rows of this launch's query chunk are indexed by token - t0
+  int t0 = 0, t1 = T;
+  if (chunk >= 0) {
+    const QChunk qc =
+        qchunk_of(cu, cu_blocks, ndoc, T, min(cu_blocks[ndoc], nb_bound), chunk, qcb);
+    t0 = qc.t0;
+    t1 = qc.t1;
+  }
+  const int tw = (int)(wid / hkv);
+  if (wid < (long long)T * hkv && tw >= t0 && tw < t1) {
+    const int t = tw, g = (int)(wid % hkv);
     const int hq = hkv * G;
     const int d = doc_of_token(cu, ndoc, t);
     const int dstart = __ldg(cu + d);
@@ -160,7 +180,7 @@ __global__ void __launch_bounds__(kRedWarps * 32)
     // ---- dQ: fixed-order sum of the slot partials ----
     for (int hh = 0; hh < G; ++hh) {
       const size_t row = (size_t)t * hq + g * G + hh;
-      const float* src = dq_part + row * K * (size_t)D + lane * PER;
+      const float* src = dq_part + ((size_t)(t - t0) * hq + g * G + hh) * K * (size_t)D + lane * PER;
       float acc[PER];
 #pragma unroll
       for (int u = 0; u < PER; ++u) acc[u] = 0.f;
@@ -228,7 +248,8 @@ __global__ void __launch_bounds__(kRedWarps * 32)
   if (threadIdx.x == 0) {
     double s = 0.0;
     for (int i = 0; i < kRedWarps; ++i) s += wkl[i];
-    kl_part[blockIdx.x] = s;
+    // a CTA may hold tokens of two query chunks: later chunks add (fixed order)
+    kl_part[blockIdx.x] = chunk > 0 ? kl_part[blockIdx.x] + s : s;
   }
 }
 
@@ -251,17 +272,22 @@ __global__ void __launch_bounds__(1024) k_kl_final(int n, const double* __restri
 
 }  // namespace
 
-cudaError_t launch_fwd_merge(const Shape& s, const int32_t* cu_seqlens, const float* o_part,
-                             const float* lse_part, uint16_t* o, uint16_t* o_res, float* lse,
-                             float* mass, cudaStream_t st) {
+cudaError_t launch_fwd_merge(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
+                             const float* o_part, const float* lse_part, uint16_t* o,
+                             uint16_t* o_res, float* lse, float* mass, int chunk,
+                             cudaStream_t st) {
   const long long warps = (long long)s.T * s.hkv;
   const int blocks = (int)((warps + kRedWarps - 1) / kRedWarps);
   if (s.d == 128)
-    k_fwd_merge<128><<<blocks, kRedWarps * 32, 0, st>>>(s.T, s.ndoc, cu_seqlens, s.hkv, s.G, s.K,
-                                                         o_part, lse_part, o, o_res, lse, mass);
+    k_fwd_merge<128><<<blocks, kRedWarps * 32, 0, st>>>(s.T, s.ndoc, cu_seqlens, cu_blocks,
+                                                         s.nb_bound, chunk, s.qc_blocks, s.hkv,
+                                                         s.G, s.K, o_part, lse_part, o, o_res,
+                                                         lse, mass);
   else
-    k_fwd_merge<64><<<blocks, kRedWarps * 32, 0, st>>>(s.T, s.ndoc, cu_seqlens, s.hkv, s.G, s.K,
-                                                        o_part, lse_part, o, o_res, lse, mass);
+    k_fwd_merge<64><<<blocks, kRedWarps * 32, 0, st>>>(s.T, s.ndoc, cu_seqlens, cu_blocks,
+                                                        s.nb_bound, chunk, s.qc_blocks, s.hkv,
+                                                        s.G, s.K, o_part, lse_part, o, o_res,
+                                                        lse, mass);
   return cudaGetLastError();
 }
 
@@ -282,22 +308,24 @@ int bwd_reduce_blocks(const Shape& s) {
   return (int)((warps + kRedWarps - 1) / kRedWarps);
 }
 
-cudaError_t launch_bwd_reduce(const Shape& s, const int32_t* cu_seqlens, const float* dq_part,
-                              const int32_t* sel_idx, const float* sel_score,
-                              const uint8_t* sel_arg, const float* plse, const float* mass,
-                              const uint16_t* k_p, float* dq, float* dq_p, double* kl_part,
-                              double* kl_loss, cudaStream_t st) {
+cudaError_t launch_bwd_reduce(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
+                              const float* dq_part, const int32_t* sel_idx,
+                              const float* sel_score, const uint8_t* sel_arg, const float* plse,
+                              const float* mass, const uint16_t* k_p, float* dq, float* dq_p,
+                              double* kl_part, double* kl_loss, int chunk, bool last,
+                              cudaStream_t st) {
   const int blocks = bwd_reduce_blocks(s);
-#define MSA_RED(DD, PP)                                                                        \
-  k_bwd_reduce<DD, PP><<<blocks, kRedWarps * 32, 0, st>>>(                                     \
-      s.T, s.ndoc, cu_seqlens, s.hkv, s.G, s.K, s.proxy_scale, s.kl_weight, dq_part, sel_idx, \
-      sel_score, sel_arg, plse, mass, k_p, dq, dq_p, kl_part)
+#define MSA_RED(DD, PP)                                                                         \
+  k_bwd_reduce<DD, PP><<<blocks, kRedWarps * 32, 0, st>>>(                                      \
+      s.T, s.ndoc, cu_seqlens, cu_blocks, s.nb_bound, chunk, s.qc_blocks, s.hkv, s.G, s.K,      \
+      s.proxy_scale, s.kl_weight, dq_part, sel_idx, sel_score, sel_arg, plse, mass, k_p, dq,     \
+      dq_p, kl_part)
   if (s.d == 128 && s.dp == 64) MSA_RED(128, 64);
   else if (s.d == 128) MSA_RED(128, 32);
   else if (s.dp == 64) MSA_RED(64, 64);
   else MSA_RED(64, 32);
 #undef MSA_RED
-  k_kl_final<<<1, 1024, 0, st>>>(blocks, kl_part, s.kl_weight, kl_loss);
+  if (last) k_kl_final<<<1, 1024, 0, st>>>(blocks, kl_part, s.kl_weight, kl_loss);
   return cudaGetLastError();
 }
 

@@ -4,6 +4,8 @@
 #include <cmath>
 #include <mutex>
 
+#include <cstdlib>
+
 #include "msa_internal.cuh"
 
 namespace msa {
@@ -96,6 +98,14 @@ msa_status check_params(const msa_params* p, Shape* s) {
   s->K = p->top_k;
   s->nb_bound = (int)nb;
   s->nchunks = (p->total_tokens + kChunkTokens - 1) / kChunkTokens;
+  s->qc_blocks = kQChunkBlocks;
+  if (const char* env = std::getenv("MSA_QUERY_CHUNK_BLOCKS")) {
+    const long v = std::strtol(env, nullptr, 10);
+    if (v > 0 && v < kQChunkBlocks) s->qc_blocks = (int)v;
+  }
+  s->nqchunks = (int)((nb + s->qc_blocks - 1) / s->qc_blocks);
+  const long long qct = (long long)s->qc_blocks * kBlock;
+  s->qc_tokens = p->total_tokens < qct ? p->total_tokens : (int)qct;
   s->softmax_scale = p->softmax_scale;
   s->proxy_scale = p->proxy_scale;
   s->kl_weight = p->kl_weight;
@@ -132,12 +142,12 @@ Workspace workspace_layout(const Shape& s, WsKind kind) {
     w.ent = take((size_t)s.T * s.hkv * (size_t)(s.K > 1 ? s.K - 1 : 1) * 4);
   }
   if (kind == kWsFwd) {
-    w.o_part = take((size_t)s.T * s.hq * s.K * s.d * 4);
-    w.lse_part = take((size_t)s.T * s.hq * s.K * 4);
+    w.o_part = take((size_t)s.qc_tokens * s.hq * s.K * s.d * 4);  // one query chunk
+    w.lse_part = take((size_t)s.qc_tokens * s.hq * s.K * 4);
   }
   if (kind == kWsBwd) {
     w.dsum = take((size_t)s.T * s.hq * 4);
-    w.dq_part = take((size_t)s.T * s.hq * s.K * s.d * 4);
+    w.dq_part = take((size_t)s.qc_tokens * s.hq * s.K * s.d * 4);  // one query chunk
     w.kl_part = take((size_t)bwd_reduce_blocks(s) * 8 + 8);
     // one record per list entry (diagonal + gathered) of every (group, block),
     // plus one tile of padding read by the last tile's bulk copy
@@ -268,11 +278,17 @@ msa_status msa_fwd(const msa_params* p, const int32_t* cu_seqlens, const uint16_
                            status, cs));
   }
   MSA_TRY(prof_mark(2, true, cs));
-  MSA_TRY(launch_fwd(s, cu_seqlens, cu_blocks, row_ptr, ent, q, k, v, o_part, lse_part, status,
-                     cs));
-  MSA_TRY(prof_mark(2, false, cs));
-  MSA_TRY(launch_fwd_merge(s, cu_seqlens, o_part, lse_part, o, o_res, lse, mass, cs));
-  g_launches += reuse ? 2 : 7;
+  // one pass per query chunk (a single pass, chunk = -1, when the batch fits one)
+  const int nq = s.nqchunks;
+  for (int c = 0; c < nq; ++c) {
+    const int chunk = nq == 1 ? -1 : c;
+    MSA_TRY(launch_fwd(s, cu_seqlens, cu_blocks, row_ptr, ent, q, k, v, o_part, lse_part, chunk,
+                       status, cs));
+    if (c == nq - 1) MSA_TRY(prof_mark(2, false, cs));
+    MSA_TRY(launch_fwd_merge(s, cu_seqlens, cu_blocks, o_part, lse_part, o, o_res, lse, mass,
+                             chunk, cs));
+  }
+  g_launches += (reuse ? 0 : 5) + 2 * nq;
   return MSA_OK;
 }
 
@@ -318,12 +334,25 @@ msa_status msa_bwd(const msa_params* p, const int32_t* cu_seqlens, const uint16_
   }
   MSA_TRY(launch_bwd_pre(s, o, o_res, dO, dsum, cs));
   MSA_TRY(prof_mark(3, true, cs));
-  MSA_TRY(launch_bwd(s, cu_seqlens, cu_blocks, row_ptr, ent, base + w.rec, q, k, v, q_p, dO, lse,
-                     dsum, mass, sel_score, sel_arg, plse, dq_part, dk, dv, dk_p, status, cs));
-  MSA_TRY(prof_mark(3, false, cs));
-  MSA_TRY(launch_bwd_reduce(s, cu_seqlens, dq_part, sel_idx, sel_score, sel_arg, plse, mass, k_p,
-                            dq, dq_p, kl_part, kl_loss, cs));
-  g_launches += reuse ? 5 : 10;
+  // one pass per query chunk; with several, dK, dV and dk_p start from zero and
+  // every pass adds its queries' share (chunk order, so the sum is deterministic)
+  const int nq = s.nqchunks;
+  if (nq > 1) {
+    MSA_TRY(cudaMemsetAsync(dk, 0, (size_t)s.T * s.hkv * s.d * 4, cs));
+    MSA_TRY(cudaMemsetAsync(dv, 0, (size_t)s.T * s.hkv * s.d * 4, cs));
+    MSA_TRY(cudaMemsetAsync(dk_p, 0, (size_t)s.T * s.hkv * s.dp * 4, cs));
+  }
+  for (int c = 0; c < nq; ++c) {
+    const int chunk = nq == 1 ? -1 : c;
+    MSA_TRY(launch_bwd(s, cu_seqlens, cu_blocks, row_ptr, ent, base + w.rec, q, k, v, q_p, dO,
+                       lse, dsum, mass, sel_score, sel_arg, plse, dq_part, dk, dv, dk_p, chunk,
+                       status, cs));
+    if (c == nq - 1) MSA_TRY(prof_mark(3, false, cs));
+    MSA_TRY(launch_bwd_reduce(s, cu_seqlens, cu_blocks, dq_part, sel_idx, sel_score, sel_arg,
+                              plse, mass, k_p, dq, dq_p, kl_part, kl_loss, chunk, c == nq - 1,
+                              cs));
+  }
+  g_launches += (reuse ? 0 : 5) + 2 + 3 * nq;
   return MSA_OK;
 }
 

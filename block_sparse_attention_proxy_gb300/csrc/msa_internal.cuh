@@ -120,7 +120,56 @@ struct Shape {
   int nb_bound;  // upper bound of KV blocks in the batch: ceil(T/128) + ndoc
   int nchunks;   // regroup chunks
   float softmax_scale, proxy_scale, kl_weight;
+  int qc_blocks; // KV blocks per query chunk (qchunk_of)
+  int nqchunks;  // query chunks of the slot partials
+  int qc_tokens; // tokens of the largest query chunk: rows of the partial buffers
 };
+
+// ---------------------------------------------------------------------------
+// Query chunks.  The per-slot partials of the forward (O, lse) and backward
+// (dQ) take T * Hq * k * d * 4 bytes each; to bound the workspace, one call
+// processes the queries in chunks of whole KV blocks: chunk c holds the
+// queries of global blocks [c * qcb, (c + 1) * qcb), so at most qcb * 128
+// tokens (qcb = kQChunkBlocks unless the environment variable
+// MSA_QUERY_CHUNK_BLOCKS sets a smaller positive value, used to test the
+// chunked path on small batches).  Partial rows are indexed by token - t0.
+// ---------------------------------------------------------------------------
+constexpr int kQChunkBlocks = 4096;
+struct QChunk {
+  int b0, b1;  // global block range
+  int t0, t1;  // token range
+};
+__device__ __forceinline__ int block_token_start(const int32_t* cu, const int32_t* cu_blocks,
+                                                 int ndoc, int gb) {
+  const int d = doc_of_block(cu_blocks, ndoc, gb);
+  return __ldg(cu + d) + (gb - cu_blocks[d]) * kBlock;
+}
+// c < 0: the whole batch in one chunk.
+__device__ __forceinline__ QChunk qchunk_of(const int32_t* cu, const int32_t* cu_blocks,
+                                            int ndoc, int T, int nbt, int c, int qcb) {
+  QChunk q;
+  if (c < 0) {
+    q.b0 = 0;
+    q.b1 = nbt;
+    q.t0 = 0;
+    q.t1 = T;
+    return q;
+  }
+  q.b0 = min(nbt, c * qcb);
+  q.b1 = min(nbt, q.b0 + qcb);
+  q.t0 = q.b0 < nbt ? block_token_start(cu, cu_blocks, ndoc, q.b0) : T;
+  q.t1 = q.b1 < nbt ? block_token_start(cu, cu_blocks, ndoc, q.b1) : T;
+  return q;
+}
+// First index i in [lo, hi) of a token-ascending list (ent = token << 4 | slot)
+// with token >= t, or hi.
+__device__ __forceinline__ int lower_bound_token(const uint32_t* ent, int lo, int hi, int t) {
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((int)(__ldg(ent + mid) >> 4) < t) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
 
 // Workspace carve-up (byte offsets, 256-byte aligned).
 struct Workspace {
@@ -165,10 +214,11 @@ cudaError_t launch_regroup(const Shape& s, const int32_t* cu_seqlens, const int3
 cudaError_t launch_fwd(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
                        const int32_t* row_ptr, const uint32_t* ent, const uint16_t* q,
                        const uint16_t* k, const uint16_t* v, float* o_part, float* lse_part,
-                       unsigned* status, cudaStream_t st);
-cudaError_t launch_fwd_merge(const Shape& s, const int32_t* cu_seqlens, const float* o_part,
-                             const float* lse_part, uint16_t* o, uint16_t* o_res, float* lse,
-                             float* mass, cudaStream_t st);
+                       int chunk, unsigned* status, cudaStream_t st);
+cudaError_t launch_fwd_merge(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
+                             const float* o_part, const float* lse_part, uint16_t* o,
+                             uint16_t* o_res, float* lse, float* mass, int chunk,
+                             cudaStream_t st);  // chunk as launch_bwd_reduce
 cudaError_t launch_bwd_pre(const Shape& s, const uint16_t* o, const uint16_t* o_res,
                            const uint16_t* dO, float* dsum, cudaStream_t st);
 cudaError_t launch_bwd(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
@@ -177,12 +227,15 @@ cudaError_t launch_bwd(const Shape& s, const int32_t* cu_seqlens, const int32_t*
                        const uint16_t* q_p, const uint16_t* dO, const float* lse,
                        const float* dsum, const float* mass, const float* sel_score,
                        const uint8_t* sel_arg, const float* plse, float* dq_part, float* dk,
-                       float* dv, float* dk_p, unsigned* status, cudaStream_t st);
-cudaError_t launch_bwd_reduce(const Shape& s, const int32_t* cu_seqlens, const float* dq_part,
-                              const int32_t* sel_idx, const float* sel_score,
-                              const uint8_t* sel_arg, const float* plse, const float* mass,
-                              const uint16_t* k_p, float* dq, float* dq_p, double* kl_part,
-                              double* kl_loss, cudaStream_t st);
+                       float* dv, float* dk_p, int chunk, unsigned* status, cudaStream_t st);
+// chunk < 0: one call over all tokens; otherwise the queries of chunk `chunk`
+// (partials indexed by token - t0); the KL scalar is produced when `last`.
+cudaError_t launch_bwd_reduce(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
+                              const float* dq_part, const int32_t* sel_idx,
+                              const float* sel_score, const uint8_t* sel_arg, const float* plse,
+                              const float* mass, const uint16_t* k_p, float* dq, float* dq_p,
+                              double* kl_part, double* kl_loss, int chunk, bool last,
+                              cudaStream_t st);
 int bwd_reduce_blocks(const Shape& s);
 
 }  // namespace msa

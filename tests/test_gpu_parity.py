@@ -207,3 +207,24 @@ def test_device_check_on_malformed_inputs():
     step.out["sel_idx"].copy_(sel)
     step.forward(dev)
     assert m.msa_get_device_status() == 6
+
+
+def test_query_chunks_match_oracle_and_single_pass(monkeypatch):
+    """The slot partials processed in query chunks of 3 KV blocks (9 chunks with
+    boundaries inside documents) agree with the oracle, and with one pass:
+    row-local outputs bit for bit, the block sums dK/dV/dk_p to rounding."""
+    w = synth.custom([700, 1100, 300, 900], 8, 2, 128, 64, 4, seed=7, structured=True)
+    inp = synth.make_inputs(w)
+    monkeypatch.setenv("MSA_QUERY_CHUNK_BLOCKS", "3")
+    g = _run(w, inp)
+    _check_all(w, inp, g)
+    monkeypatch.delenv("MSA_QUERY_CHUNK_BLOCKS")
+    one = _run(w, inp)
+    for n in ("sel_idx", "sel_arg", "o", "o_res", "lse", "mass", "dq", "dq_p"):
+        assert torch.equal(g[n], one[n]), n
+    for n in ("dk", "dv", "dk_p"):
+        # the chunks' fp32 partial sums are added in another association
+        scale = float(one[n].abs().max())
+        diff = float((g[n] - one[n]).abs().max())
+        assert diff <= 1e-5 * max(1.0, scale), (n, diff, scale)
+    assert abs(float(g["kl_loss"][0]) - float(one["kl_loss"][0])) <= 1e-9 * max(1.0, abs(float(one["kl_loss"][0])))
