@@ -1,5 +1,6 @@
-"""Full-size parity for the bench workloads, in the launch configuration
-bench.py times (one MSAStep: select, forward, backward through the C ABI).
+"""Full-size parity for the bench workloads (128k, 512k and 1M tokens; the
+1M step runs in two query chunks), in the launch configuration bench.py times
+(one MSAStep: select, forward, backward through the C ABI).
 
 The oracle cannot run every row of a 128k-token step, so it checks:
   * 256 seeded query rows (rows 0 and T-1 included): selection (exact outside
@@ -27,7 +28,7 @@ def _host_inputs(inp):
     return cpu
 
 
-@pytest.mark.parametrize("name", ["128k"])
+@pytest.mark.parametrize("name", ["128k", "512k", "1m"])
 def test_full_size_sampled(name):
     import block_sparse_attention_proxy_gb300 as m
     from block_sparse_attention_proxy_gb300.step import MSAStep, params_for
