@@ -378,6 +378,8 @@ def run_ours(args):
         tokens_per_s=round(w.total_tokens * world / ms * 1e3, 1),
         work_tflops=round((fl + 2.0 * w.dp * w.hkv * c["causal"]) * world / ms / 1e9, 3),
         frac_of_bf16_peak=round(value / world / peaks["bf16_tflops"], 4),
+        frac_of_bf16_sustained=round(value / world / peaks["bf16_tflops_sustained"], 4),
+        device_peak_gb=round(torch.cuda.max_memory_allocated() / 1e9, 1),
         roofline=roofline, kernels=per_kernel,
         calls_ms={k: round(v, 3) for k, v in calls.items()},
         cpu_baseline=cpu, e2e=e2e, gpu_launches=int(launches), clocks=clk,

@@ -134,7 +134,7 @@ struct Shape {
 // MSA_QUERY_CHUNK_BLOCKS sets a smaller positive value, used to test the
 // chunked path on small batches).  Partial rows are indexed by token - t0.
 // ---------------------------------------------------------------------------
-constexpr int kQChunkBlocks = 4096;
+constexpr int kQChunkBlocks = 2048;
 struct QChunk {
   int b0, b1;  // global block range
   int t0, t1;  // token range
