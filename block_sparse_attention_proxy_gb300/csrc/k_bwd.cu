@@ -224,8 +224,7 @@ __global__ void __launch_bounds__(128) k_bwd_prep(const BwdArgs a) {
 
 template <int D, int G, int DP>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    k_bwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    k_bwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
           const __grid_constant__ CUtensorMap tm_qp, const BwdArgs a) {
   using C = BwdCfg<D, G, DP>;
   constexpr int TPT = C::TPT, TPL = C::TPL, NQ = C::kNQ, NM = C::kNM, NCH = D / 64;
@@ -716,8 +715,7 @@ cudaError_t launch_bwd_t(const Shape& s, const CUtensorMap* m, const BwdArgs& a,
   e = cudaFuncSetAttribute(k_bwd<D, G, DP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmem);
   if (e != cudaSuccess) return e;
-  k_bwd<D, G, DP><<<s.nb_bound * s.hkv, kBwdThreads, C::kSmem, st>>>(m[0], m[1], m[2], m[3], m[4],
-                                                                      a);
+  k_bwd<D, G, DP><<<s.nb_bound * s.hkv, kBwdThreads, C::kSmem, st>>>(m[0], m[1], m[2], a);
   return cudaGetLastError();
 }
 
@@ -740,13 +738,12 @@ cudaError_t launch_bwd(const Shape& s, const int32_t* cu_seqlens, const int32_t*
                        const float* dsum, const float* mass, const float* sel_score,
                        const uint8_t* sel_arg, const float* plse, float* dq_part, float* dk,
                        float* dv, float* dk_p, int chunk, unsigned* status, cudaStream_t st) {
-  CUtensorMap m[5];
+  // K, V and q_p rows by TMA; Q and dO rows are gathered by cp.async in the kernel
+  CUtensorMap m[3];
   cudaError_t e;
-  if ((e = make_tmap_3d(&m[0], q, s.d, s.hq, s.T, 64, s.G, 1, 128)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&m[1], dO, s.d, s.hq, s.T, 64, s.G, 1, 128)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&m[2], k, s.d, s.hkv, s.T, 64, 1, 128, 128)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&m[3], v, s.d, s.hkv, s.T, 64, 1, 128, 128)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&m[4], q_p, s.dp, s.hkv, s.T, s.dp, 1, 1, 0)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&m[0], k, s.d, s.hkv, s.T, 64, 1, 128, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&m[1], v, s.d, s.hkv, s.T, 64, 1, 128, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&m[2], q_p, s.dp, s.hkv, s.T, s.dp, 1, 1, 0)) != cudaSuccess) return e;
   BwdArgs a{cu_seqlens, cu_blocks, row_ptr,    ent,        rec,          lse,         dsum,
             mass,       sel_score, sel_arg,    plse,       s.ndoc,       s.T,         s.hq,
             s.hkv,      s.K,       s.nb_bound, s.softmax_scale, s.proxy_scale, s.kl_weight,
