@@ -28,7 +28,11 @@ listed as a reading in the design notes):
   2. block max-pool   S_b = max over keys of block b with key <= i; a_b = the
                       lowest key attaining it (stored as offset in the block)
   3. selection        the diagonal block j is always kept; of b < j keep all if
-                      j <= k-1, else the k-1 largest S_b, ties to the lower b
+                      j <= k-1, else the k-1 largest S_b, ties to the lower b.
+                      Block pattern (window w, dilation s; w = 0 is the plain
+                      rule): the blocks F = {j - s u : 1 <= u <= w, j - s u >= 0}
+                      are kept as well, inside the k slots, and the top-k
+                      choice fills the other k-1-|F| slots from b < j, b not in F
   4. mask             M[i,key] = key <= i and key // B selected
   5. attention        z = softmax_scale * q[t,h] . k[key,g] on M,
                       LSE = logsumexp z, P = exp(z - LSE), O = sum P v
@@ -70,6 +74,8 @@ class OracleParams:
     softmax_scale: float = 1.0
     proxy_scale: float = 1.0
     kl_weight: float = 1.0
+    window: int = 0
+    dilation: int = 1
 
     @property
     def group(self) -> int:
@@ -142,22 +148,38 @@ def pooled_proxy_scores(q_p_doc: np.ndarray, k_p_doc: np.ndarray, rows: np.ndarr
 # ---------------------------------------------------------------------------
 # step 3: top-k selection with the diagonal always kept
 # ---------------------------------------------------------------------------
-def select_from_pooled(S_row: np.ndarray, j: int, k: int):
+def forced_blocks(j: int, window: int, dilation: int) -> list:
+    """The always-kept earlier blocks of block j under a block pattern of
+    `window` blocks spaced `dilation` apart: j - dilation * u for u = 1..window,
+    those >= 0.  The pattern is configurable by window size and dilation
+    ("Flash-MSA: Ein Training mit einer Million Tokens ohne hohe
+    Rechenkosten", keelcrux.com, section "Under the hood"); the set itself is
+    this library's reading of those two words."""
+    return [j - dilation * u for u in range(1, window + 1) if j - dilation * u >= 0]
+
+
+def select_from_pooled(S_row: np.ndarray, j: int, k: int, window: int = 0, dilation: int = 1):
     """Selection for one (row, group).  S_row holds S_b for b = 0..j.
 
     Returns (sel, gap): sel is a length-k list of block ids, ascending, the
-    diagonal j included, padded with -1; gap is S of the (k-1)-th best minus S
-    of the k-th best among b < j (inf when every candidate is taken).
+    diagonal j included, padded with -1; gap is, among the candidates the
+    top-k choice ranks (b < j outside the always-kept window), S of the last
+    one taken minus S of the first one left (inf when no choice is made).
     """
-    cand = np.asarray(S_row[:j], dtype=np.float64)
-    if j <= k - 1:
-        chosen = list(range(j))
+    forced = forced_blocks(j, window, dilation)
+    if len(forced) > k - 1:
+        raise ValueError("the always-kept window does not fit in top_k - 1 slots")
+    cand_ids = [b for b in range(j) if b not in forced]
+    free = k - 1 - len(forced)
+    if len(cand_ids) <= free:
+        chosen = cand_ids
         gap = math.inf
     else:
+        cand = np.asarray([S_row[b] for b in cand_ids], dtype=np.float64)
         order = np.argsort(-cand, kind="stable")  # descending score, ties by lower b
-        chosen = [int(b) for b in order[: k - 1]]
-        gap = float(cand[order[k - 2]] - cand[order[k - 1]])
-    sel = sorted(chosen) + [j]
+        chosen = [cand_ids[int(n)] for n in order[:free]]
+        gap = math.inf if free == 0 else float(cand[order[free - 1]] - cand[order[free]])
+    sel = sorted(chosen + forced) + [j]
     sel = sel + [-1] * (k - len(sel))
     return sel, gap
 
@@ -170,7 +192,7 @@ def select_blocks(S: np.ndarray, rows: np.ndarray, prm: OracleParams):
     for n, i in enumerate(rows):
         j = int(i) // prm.block
         for g in range(prm.hkv):
-            s, gp = select_from_pooled(S[n, g, : j + 1], j, prm.top_k)
+            s, gp = select_from_pooled(S[n, g, : j + 1], j, prm.top_k, prm.window, prm.dilation)
             sel[n, g] = s
             gap[n, g] = gp
     return sel, gap
@@ -338,7 +360,7 @@ def row_reference(inputs: dict, prm: OracleParams, t: int, sel_override=None, ar
         S = blocks.max(axis=1)
         A = blocks.argmax(axis=1)
         res["pooled"][g] = S
-        own, gap = select_from_pooled(S, j, K)
+        own, gap = select_from_pooled(S, j, K, prm.window, prm.dilation)
         res["gap"][g] = gap
         own_arr = np.asarray(own)
         res["own_arg"][g] = np.where(own_arr >= 0, A[np.maximum(own_arr, 0)], 0)

@@ -138,6 +138,78 @@ def test_selection_ties_go_to_lower_block():
 
 
 # ---------------------------------------------------------------------------
+# block pattern: an always-kept window of w blocks spaced s apart
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(4))
+def test_window_selection_matches_brute_force_subsets(seed):
+    """With a window (w, s), the selection is, among the min(j, k-1)-subsets of
+    earlier blocks that hold every block at distance s*u (u = 1..w) behind j,
+    the one with the largest score sum (distinct scores), plus the diagonal."""
+    rng = np.random.default_rng(100 + seed)
+    for j in range(0, 12):
+        for k in (2, 3, 4, 6):
+            for w in range(0, k):
+                for s in (1, 2, 3):
+                    S = rng.normal(size=j + 1)
+                    sel, gap = select_from_pooled(S, j, k, window=w, dilation=s)
+                    must = {b for b in range(j) if (j - b) % s == 0 and (j - b) // s <= w}
+                    size = min(j, k - 1)
+                    subsets = [c for c in itertools.combinations(range(j), size) if must <= set(c)]
+                    want = sorted(max(subsets, key=lambda c: sum(S[list(c)])))
+                    assert sel == want + [j] + [-1] * (k - 1 - size), (j, k, w, s)
+                    free = sorted((S[b] for b in range(j) if b not in must), reverse=True)
+                    nfree = size - len(must)
+                    if nfree == 0 or len(free) <= nfree:
+                        assert gap == math.inf
+                    else:
+                        assert abs(gap - (free[nfree - 1] - free[nfree])) < 1e-15
+
+
+def test_window_must_fit_in_top_k():
+    with pytest.raises(ValueError):
+        select_from_pooled(np.zeros(8), 7, 3, window=3, dilation=1)
+    # a window reaching past the document start keeps only the blocks that exist
+    assert select_from_pooled(np.zeros(8), 7, 3, window=2, dilation=5)[0] == [0, 2, 7]
+
+
+def _sdpa_local(inp, hq, hkv, block, nblocks):
+    """Causal GQA attention restricted to keys in the last `nblocks` blocks of
+    the query (its own included), per document, with torch's SDPA and an
+    explicit boolean mask (float64 CPU); outputs and gradients of sum(O * dO)."""
+    G = hq // hkv
+    cu = inp["cu_seqlens"].tolist()
+    res = [[], [], [], []]
+    for a, b in zip(cu[:-1], cu[1:]):
+        L = b - a
+        pos = torch.arange(L)
+        keep = (pos[None, :] <= pos[:, None]) & (pos[None, :] // block > pos[:, None] // block - nblocks)
+        q = inp["q"][a:b].double().transpose(0, 1).clone().requires_grad_(True)
+        k = inp["k"][a:b].double().transpose(0, 1).clone().requires_grad_(True)
+        v = inp["v"][a:b].double().transpose(0, 1).clone().requires_grad_(True)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q, k.repeat_interleave(G, dim=0), v.repeat_interleave(G, dim=0), attn_mask=keep,
+            scale=1.0)
+        (o * inp["dO"][a:b].double().transpose(0, 1)).sum().backward()
+        for lst, x in zip(res, (o.detach(), q.grad, k.grad, v.grad)):
+            lst.append(x.transpose(0, 1))
+    return [torch.cat(x).numpy() for x in res]
+
+
+def test_full_window_is_sliding_window_attention():
+    """w = k-1, s = 1 keeps the last k blocks whatever the proxy says: the
+    attention is sliding-window attention over k blocks."""
+    hq, hkv, d, dp, block, k = 4, 2, 8, 4, 16, 3
+    inp = _inputs([150, 77, 16], hq, hkv, d, dp, seed=21)
+    prm = OracleParams(hq=hq, hkv=hkv, d=d, dp=dp, top_k=k, block=block, window=k - 1)
+    ref = msa_reference(inp, prm)
+    o, dq, dk, dv = _sdpa_local(inp, hq, hkv, block, k)
+    np.testing.assert_allclose(ref["o"], o, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(ref["dq"], dq, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(ref["dk"], dk, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(ref["dv"], dv, rtol=1e-9, atol=1e-11)
+
+
+# ---------------------------------------------------------------------------
 # gradients: central finite differences of the forward (fp64)
 # ---------------------------------------------------------------------------
 def _loss(inp, prm, sel, arg, mass0):
@@ -220,10 +292,12 @@ def _autograd_step(inp, sel, prm):
     return {("d" + n): t[n].grad.numpy() for n in t}, float(total)
 
 
-def test_gradients_match_autograd():
+@pytest.mark.parametrize("window,dilation", [(0, 1), (1, 2)])
+def test_gradients_match_autograd(window, dilation):
     hq, hkv, d, dp, block, k = 4, 2, 8, 4, 16, 3
     inp = _inputs([90, 161], hq, hkv, d, dp, seed=13)
-    prm = _prm(hq, hkv, d, dp, k, block)
+    prm = OracleParams(hq=hq, hkv=hkv, d=d, dp=dp, top_k=k, block=block, window=window,
+                       dilation=dilation)
     ref = msa_reference(inp, prm)
     grads, _ = _autograd_step(inp, ref["sel_idx"], prm)
     for n in ("dq", "dk", "dv", "dq_p", "dk_p"):
