@@ -28,10 +28,15 @@ __all__ = [
 
 
 def make_params(total_tokens, num_docs, max_seqlen, hq, hkv, d, dp, top_k, block=128,
-                softmax_scale=1.0, proxy_scale=1.0, kl_weight=1.0, flags=0) -> MsaParams:
-    return MsaParams(int(total_tokens), int(num_docs), int(max_seqlen), int(hq), int(hkv), int(d),
-                     int(dp), int(block), int(top_k), float(softmax_scale), float(proxy_scale),
-                     float(kl_weight), int(flags))
+                softmax_scale=1.0, proxy_scale=1.0, kl_weight=1.0, flags=0, window=0,
+                dilation=1) -> MsaParams:
+    """msa_params; window/dilation set the always-kept block pattern (0: none)."""
+    return MsaParams(total_tokens=int(total_tokens), num_docs=int(num_docs),
+                     max_seqlen=int(max_seqlen), hq=int(hq), hkv=int(hkv), d=int(d), dp=int(dp),
+                     block=int(block), top_k=int(top_k), window=int(window),
+                     dilation=int(dilation), softmax_scale=float(softmax_scale),
+                     proxy_scale=float(proxy_scale), kl_weight=float(kl_weight),
+                     flags=int(flags))
 
 
 def _ptr(t) -> ctypes.c_void_p:

@@ -47,6 +47,8 @@ class MsaParams(ctypes.Structure):
         ("dp", ctypes.c_int32),
         ("block", ctypes.c_int32),
         ("top_k", ctypes.c_int32),
+        ("window", ctypes.c_int32),
+        ("dilation", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
         ("proxy_scale", ctypes.c_float),
         ("kl_weight", ctypes.c_float),

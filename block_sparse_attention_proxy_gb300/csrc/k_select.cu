@@ -19,6 +19,13 @@
 // into a 256-column TMEM accumulator, and each warpgroup takes every other
 // step with its own accumulator.  The fixed cost of a step (barrier hand-offs,
 // commits) is paid once per two blocks.
+//
+// Block pattern: with a window (w, s) the blocks J - s*u, u = 1..w, are kept
+// whatever their score; the pattern is configurable by window size and
+// dilation ("Flash-MSA: Ein Training mit einer Million Tokens ohne hohe
+// Rechenkosten", keelcrux.com, "Under the hood").  Their scores and argmaxes
+// go to slots of their own in shared memory, they never enter the ranked list,
+// and the ranked list fills the other k-1-|window| slots.
 #include <cfloat>
 
 #include "msa_internal.cuh"
@@ -104,6 +111,7 @@ struct SelArgs {
   const int32_t* cu;
   const int32_t* cu_blocks;
   int ndoc, T, hkv, K, nb_bound;
+  int window, dilation;  // always-kept blocks J - dilation * u, u = 1..window
   float proxy_scale;
   int32_t* sel_idx;
   float* sel_score;
@@ -128,7 +136,9 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   uint32_t* m_id = reinterpret_cast<uint32_t*>(m_sc + CAP * 128);           // [CAP][128]
   float* d_sc = reinterpret_cast<float*>(m_id + CAP * 128);                 // [128]
   uint32_t* d_id = reinterpret_cast<uint32_t*>(d_sc + 128);                 // [128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(d_id + 128);
+  float* f_sc = reinterpret_cast<float*>(d_id + 128);          // [CAP][128] always-kept blocks
+  uint32_t* f_id = reinterpret_cast<uint32_t*>(f_sc + CAP * 128);           // [CAP][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(f_id + CAP * 128);
   // bars: 0 qfull | 1..S kvfull | S+1..2S kvempty | 2S+1..2S+2 accfull | 2S+3..2S+4 accempty
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kSelStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
@@ -259,6 +269,10 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         const bool last = u == 1 || n + 1 >= nblk;
         const uint32_t tb = tbase + lane_off + acc * 256 + u * 128;
         const bool diag = (n == J);
+        // block of the always-kept window (warp-uniform): J - n = dilation * u, 1 <= u <= window
+        const int dj = J - n;
+        const bool forced = a.window > 0 && dj > 0 && dj <= a.window * a.dilation &&
+                            dj % a.dilation == 0;
         // argmax bookkeeping for every block (ARG), else for the diagonal block only
         const bool track = ARG || diag;  // warp-uniform
         // The 32 scores of the chunk holding the row maximum stay in registers (first chunk
@@ -298,7 +312,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
           }
         }
         // blocks reach this warpgroup in increasing order, so ties keep the older entry
-        const bool need = diag || best * ps > sc[CAP - 1];
+        const bool need = diag || forced || best * ps > sc[CAP - 1];
         int arg = 0;
         if (need && track) {
           int aa = 31;
@@ -315,6 +329,10 @@ __global__ void __launch_bounds__(kSelThreads, 1)
           dsv = best * ps;
           dav = ((uint32_t)n << 8) | (uint32_t)arg;
           handled_diag = true;
+        } else if (forced) {  // kept whatever its score: a slot of its own, not the ranking
+          const int u = dj / a.dilation - 1;
+          f_sc[u * 128 + row] = best * ps;
+          f_id[u * 128 + row] = ((uint32_t)n << 8) | (uint32_t)arg;
         } else if (need) {
           list_insert_newer<CAP>(sc, id, best * ps, ((uint32_t)n << 8) | (uint32_t)arg);
         }
@@ -343,15 +361,25 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       dav = d_id[row];
       const int K = a.K;
       const int nsel = min(J, K - 1);  // off-diagonal blocks kept
+      const int nf = a.window > 0 ? min(a.window, J / a.dilation) : 0;  // always kept
+      const int ntop = nsel - nf;      // chosen by score from the other earlier blocks
       uint8_t tie = 0;
-      if (J > K - 1 && K >= 2) {
-        float s_km2 = 0.f, s_km1 = 0.f;
+      if (J > K - 1 && ntop >= 1) {  // a choice was made: last taken vs first left
+        float s_last = 0.f, s_next = 0.f;
 #pragma unroll
         for (int i = 0; i < CAP; ++i) {
-          if (i == K - 2) s_km2 = sc[i];
-          if (i == K - 1) s_km1 = sc[i];
+          if (i == ntop - 1) s_last = sc[i];
+          if (i == ntop) s_next = sc[i];
         }
-        tie = (s_km2 - s_km1) < kTieBand ? 1 : 0;
+        tie = (s_last - s_next) < kTieBand ? 1 : 0;
+      }
+      // the always-kept blocks take list entries ntop .. nsel-1
+#pragma unroll
+      for (int i = 0; i < CAP; ++i) {
+        if (i >= ntop && i < nsel) {
+          sc[i] = f_sc[(i - ntop) * 128 + row];
+          id[i] = f_id[(i - ntop) * 128 + row];
+        }
       }
       // plse over the selection (nsel best + diagonal)
       float mx = dsv;
@@ -424,8 +452,8 @@ template <int DP, int CAP, bool ARG>
 cudaError_t launch_sel_t(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
                          const SelArgs& a, cudaStream_t st) {
   using C = SelCfg<DP>;
-  const size_t smem = 1024 + (1 + 2 * kSelStages) * C::kTileBytes + CAP * 128 * 8 + 128 * 8 +
-                      (2 * kSelStages + 5) * 8 + 16;
+  const size_t smem = 1024 + (1 + 2 * kSelStages) * C::kTileBytes + 2 * CAP * 128 * 8 +
+                      128 * 8 + (2 * kSelStages + 5) * 8 + 16;
   cudaError_t e = cudaFuncSetAttribute(k_select<DP, CAP, ARG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -452,8 +480,9 @@ cudaError_t launch_select(const Shape& s, const int32_t* cu_seqlens, const int32
   cudaError_t e;
   if ((e = make_tmap_3d(&mq, q_p, s.dp, s.hkv, s.T, s.dp, 1, 128, sw)) != cudaSuccess) return e;
   if ((e = make_tmap_3d(&mk, k_p, s.dp, s.hkv, s.T, s.dp, 1, 256, sw)) != cudaSuccess) return e;
-  SelArgs a{cu_seqlens, cu_blocks, s.ndoc, s.T, s.hkv, s.K, s.nb_bound, s.proxy_scale,
-            sel_idx,    sel_score, sel_arg, plse,   tie,  status};
+  SelArgs a{cu_seqlens, cu_blocks, s.ndoc,   s.T,         s.hkv, s.K,
+            s.nb_bound, s.window,  s.dilation, s.proxy_scale, sel_idx, sel_score,
+            sel_arg,    plse,      tie,    status};
   const int cap = s.K <= 4 ? 4 : (s.K <= 8 ? 8 : 16);
   if (s.dp == 64) {
     if (cap == 4) return launch_sel_a<64, 4>(s, mq, mk, a, with_arg, st);

@@ -85,6 +85,7 @@ msa_status check_params(const msa_params* p, Shape* s) {
   if (G != 1 && G != 2 && G != 4 && G != 8) return MSA_ERR_UNSUPPORTED;
   if (p->hkv > 255 || p->hq > 255) return MSA_ERR_UNSUPPORTED;
   if (p->top_k < 1 || p->top_k > kMaxTopK) return MSA_ERR_UNSUPPORTED;
+  if (p->window < 0 || p->window > p->top_k - 1 || p->dilation < 0) return MSA_ERR_INVALID_ARG;
   const long long nb = (long long)(p->total_tokens + kBlock - 1) / kBlock + p->num_docs;
   if (nb > kMaxBlocks) return MSA_ERR_UNSUPPORTED;
   s->T = p->total_tokens;
@@ -96,6 +97,10 @@ msa_status check_params(const msa_params* p, Shape* s) {
   s->d = p->d;
   s->dp = p->dp;
   s->K = p->top_k;
+  s->window = p->window;
+  // any spacing beyond the largest block index keeps no block; clamping keeps
+  // window * dilation inside int
+  s->dilation = p->dilation < 1 ? 1 : (p->dilation > kMaxBlocks ? kMaxBlocks : p->dilation);
   s->nb_bound = (int)nb;
   s->nchunks = (p->total_tokens + kChunkTokens - 1) / kChunkTokens;
   s->qc_blocks = kQChunkBlocks;

@@ -117,6 +117,7 @@ __host__ __device__ constexpr int bwd_rec_bytes(int G) { return 16 + ((8 * G + 1
 // ---------------------------------------------------------------------------
 struct Shape {
   int T, ndoc, max_seqlen, hq, hkv, G, d, dp, K;
+  int window, dilation;  // block pattern: blocks j - dilation * u, u = 1..window, always kept
   int nb_bound;  // upper bound of KV blocks in the batch: ceil(T/128) + ndoc
   int nchunks;   // regroup chunks
   float softmax_scale, proxy_scale, kl_weight;

@@ -43,7 +43,7 @@ class MSAFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q, k, v, q_p, k_p, cu_seqlens, top_k: int, softmax_scale: float,
-                proxy_scale: float, kl_weight: float):
+                proxy_scale: float, kl_weight: float, window: int, dilation: int):
         for t in (q, k, v, q_p, k_p):
             if t.dtype != torch.bfloat16 or not t.is_cuda:
                 raise TypeError("q, k, v, q_p, k_p must be bf16 CUDA tensors")
@@ -52,7 +52,7 @@ class MSAFunction(torch.autograd.Function):
         cu = cu_seqlens.to(torch.int32).contiguous()
         prm = params_for([int(x) for x in cu.tolist()], hq, hkv, d, dp, top_k,
                          softmax_scale=softmax_scale, proxy_scale=proxy_scale,
-                         kl_weight=kl_weight)
+                         kl_weight=kl_weight, window=window, dilation=dilation)
         ws = _workspace_for(prm, q.device)
         out = allocate_outputs(prm, q.device)
         q, k, v, q_p, k_p = (t.contiguous() for t in (q, k, v, q_p, k_p))
@@ -76,14 +76,18 @@ class MSAFunction(torch.autograd.Function):
                 o["sel_idx"], o["sel_score"], o["sel_arg"], o["plse"], o["dq"], o["dk"], o["dv"],
                 o["dq_p"], o["dk_p"], o["kl_loss"], ws, ctx.stream)
         _last_kl[0] = o["kl_loss"]
-        return o["dq"], o["dk"], o["dv"], o["dq_p"], o["dk_p"], None, None, None, None, None
+        return (o["dq"], o["dk"], o["dv"], o["dq_p"], o["dk_p"], None, None, None, None, None,
+                None, None)
 
 
 def msa_attention(q, k, v, q_p, k_p, cu_seqlens, top_k: int, softmax_scale: float = 1.0,
-                  proxy_scale: float = 1.0, kl_weight: float = 1.0) -> torch.Tensor:
-    """Block-sparse MSA attention over a packed varlen batch (see module docstring)."""
+                  proxy_scale: float = 1.0, kl_weight: float = 1.0, window: int = 0,
+                  dilation: int = 1) -> torch.Tensor:
+    """Block-sparse MSA attention over a packed varlen batch (see module docstring).
+    window/dilation: blocks j - dilation * u (u = 1..window) are always kept,
+    inside the top_k slots (window <= top_k - 1; 0 keeps none)."""
     return MSAFunction.apply(q, k, v, q_p, k_p, cu_seqlens, int(top_k), float(softmax_scale),
-                             float(proxy_scale), float(kl_weight))
+                             float(proxy_scale), float(kl_weight), int(window), int(dilation))
 
 
 def last_kl_loss() -> torch.Tensor | None:

@@ -28,6 +28,15 @@
  *         inside block b (treated as a constant target),
  * and the loss kl_weight * sum_{t,g} KL_{t,g}.
  *
+ * Block pattern (window w, dilation s): besides the diagonal, the blocks
+ * j - s*u for u = 1..w (those >= 0) are always kept; they take w of the k
+ * slots and the top-k choice fills the remaining k-1-w from the other earlier
+ * blocks (all of them when they fit).  w = 0 is the plain rule.  The pattern
+ * is configurable by window size and dilation ("Flash-MSA: Ein Training mit
+ * einer Million Tokens ohne hohe Rechenkosten", keelcrux.com, section "Under
+ * the hood"); the set above is this library's reading of those two words.
+ * With w = k-1 and s = 1 the selection is a sliding window of k blocks.
+ *
  * Notation: T total tokens, Hq query heads, Hkv KV heads (groups), G = Hq/Hkv,
  * d head dim, dp proxy dim, B = 128 block size, K = top_k (diagonal included).
  * A token at doc-local position i lies in block j = i / B.  Blocks restart at
@@ -45,8 +54,10 @@
  *   sel_arg           [T, Hkv, K]    uint8 offset inside the block of the key
  *                                    attaining S_b (lowest such key)
  *   plse              [T, Hkv]       fp32 logsumexp of S_b over the selection
- *   tie               [T, Hkv]       uint8 1 when the (k-1)-th and k-th best
- *                                    candidate scores differ by less than 1e-3
+ *   tie               [T, Hkv]       uint8 1 when the last candidate the top-k
+ *                                    choice takes and the first it leaves
+ *                                    (always-kept blocks are not candidates)
+ *                                    differ in score by less than 1e-3
  *   o_res             [T, Hq, d]     bf16 rounding residual of o: bf16(O - o) for the
  *                                    fp32 result O, so o + o_res carries ~16
  *                                    mantissa bits (saved for msa_bwd, whose
@@ -95,6 +106,9 @@ typedef struct msa_params {
   int32_t d, dp;        /* head dim, proxy dim */
   int32_t block;        /* KV block size; must be 128 */
   int32_t top_k;        /* selected blocks per (token, group), diagonal included */
+  int32_t window;       /* block pattern: always-kept earlier blocks, 0 <= window <= top_k - 1
+                           (0: none; see "Block pattern" above) */
+  int32_t dilation;     /* block pattern: spacing of those blocks, >= 0 (0 is read as 1) */
   float softmax_scale;  /* multiplies q . k (1.0 when q is pre-scaled) */
   float proxy_scale;    /* multiplies q_p . k_p (1.0 when q_p is pre-scaled) */
   float kl_weight;      /* lambda of the proxy KL loss */

@@ -42,24 +42,30 @@ def assert_close(name, gpu, ref, cos_min=COS_MIN, abs_max=ABS_MAX):
     return c, e
 
 
-def check_selection_row(gpu_sel, own_sel, pooled, j, k):
+def check_selection_row(gpu_sel, own_sel, pooled, j, k, window=0, dilation=1):
     """One (row, group): GPU and oracle block lists must agree, or differ only in
     blocks whose oracle pooled score is within TIE_BAND of the selection boundary.
-    Returns True when the row is an excused tie."""
+    With a block pattern (window, dilation) the always-kept blocks must be in
+    the GPU's list and are not ranked.  Returns True when the row is an excused tie."""
     gpu_sel = [int(x) for x in gpu_sel]
     own_sel = [int(x) for x in own_sel]
+    n_off = min(j, k - 1)
+    kept = {j - dilation * u for u in range(1, window + 1) if j - dilation * u >= 0}
+    assert kept <= set(gpu_sel[:n_off]), (gpu_sel, sorted(kept))
     if gpu_sel == own_sel:
         return False
     # structure: ascending, diagonal last, -1 padding
-    n_off = min(j, k - 1)
     assert gpu_sel[n_off] == j and all(x == -1 for x in gpu_sel[n_off + 1:]), gpu_sel
     assert gpu_sel[:n_off] == sorted(set(gpu_sel[:n_off])), gpu_sel
+    free = n_off - len(kept)  # slots the ranking fills
+    ranked = np.asarray([b for b in range(j) if b not in kept])
+    assert free >= 1 and len(ranked) > free, f"no choice to tie on: {gpu_sel} vs {own_sel}"
     cand = np.asarray(pooled[:j], np.float64)
-    srt = np.sort(cand)[::-1]
-    lo = srt[k - 1] if len(srt) > k - 1 else -np.inf   # best excluded
-    hi = srt[k - 2]                                      # worst included
+    srt = np.sort(cand[ranked])[::-1]
+    lo = srt[free]        # best excluded
+    hi = srt[free - 1]    # worst included
     assert hi - lo < TIE_BAND, f"selection differs outside the tie band: {gpu_sel} vs {own_sel}"
     diff = set(gpu_sel[:n_off]) ^ set(own_sel[:n_off])
     for b in diff:
-        assert lo - TIE_BAND <= cand[b] <= hi + TIE_BAND, (b, cand[b], lo, hi)
+        assert b not in kept and lo - TIE_BAND <= cand[b] <= hi + TIE_BAND, (b, cand[b], lo, hi)
     return True

@@ -84,8 +84,22 @@ def test_host_errors_before_any_launch(m):
 
 
 def test_params_layout_matches_header(m):
-    # 9 int32, 3 float, 1 uint32
-    assert ctypes.sizeof(m.MsaParams) == 13 * 4
+    # 11 int32, 3 float, 1 uint32, in the header's order
+    assert ctypes.sizeof(m.MsaParams) == 15 * 4
+    names = [f[0] for f in m.MsaParams._fields_]
+    assert names == ["total_tokens", "num_docs", "max_seqlen", "hq", "hkv", "d", "dp", "block",
+                     "top_k", "window", "dilation", "softmax_scale", "proxy_scale", "kl_weight",
+                     "flags"]
+    assert m.MsaParams.window.offset == 9 * 4 and m.MsaParams.flags.offset == 14 * 4
+
+
+def test_block_pattern_params_checked_on_host(m):
+    ok = m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4, window=3, dilation=2)
+    assert m.msa_fwd_workspace_size(ok) > 0
+    zero_dil = m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4, window=2, dilation=0)
+    assert m.msa_fwd_workspace_size(zero_dil) == m.msa_fwd_workspace_size(ok)  # 0 reads as 1
+    for bad in (dict(window=4), dict(window=-1), dict(window=1, dilation=-2)):
+        assert m.msa_select_workspace_size(m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4, **bad)) == 0
 
 
 def test_launch_counter_starts_at_zero_without_gpu(m):

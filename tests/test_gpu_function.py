@@ -8,31 +8,32 @@ import synth
 pytestmark = pytest.mark.gpu
 
 
-def _step_outputs(w, dev):
+def _step_outputs(w, dev, **pattern):
     from block_sparse_attention_proxy_gb300.step import MSAStep, params_for
 
-    prm = params_for(dev["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k)
+    prm = params_for(dev["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k, **pattern)
     st = MSAStep(prm)
     st(dev)
     return {k: v.clone() for k, v in st.out.items()}
 
 
-def _autograd(w, dev):
+def _autograd(w, dev, **pattern):
     from block_sparse_attention_proxy_gb300.function import msa_attention
 
     leaves = {n: dev[n].clone().requires_grad_(True) for n in ("q", "k", "v", "q_p", "k_p")}
     o = msa_attention(leaves["q"], leaves["k"], leaves["v"], leaves["q_p"], leaves["k_p"],
-                      dev["cu_seqlens"], w.top_k)
+                      dev["cu_seqlens"], w.top_k, **pattern)
     return o, leaves
 
 
-def test_autograd_matches_step():
+@pytest.mark.parametrize("pattern", [{}, dict(window=2, dilation=2)], ids=["plain", "window"])
+def test_autograd_matches_step(pattern):
     from block_sparse_attention_proxy_gb300.function import last_kl_loss
 
     w = synth.custom([900, 1300], 8, 2, 128, 64, 4, seed=31, structured=True)
     dev = {k: v.cuda() for k, v in synth.make_inputs(w).items()}
-    ref = _step_outputs(w, dev)
-    o, leaves = _autograd(w, dev)
+    ref = _step_outputs(w, dev, **pattern)
+    o, leaves = _autograd(w, dev, **pattern)
     assert torch.equal(o, ref["o"])
     o.backward(dev["dO"])
     for n, g in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("q_p", "dq_p"), ("k_p", "dk_p")):

@@ -2,7 +2,8 @@
 
 Workloads: the 1024-token tiny step, the 32768-token varlen batch, and small
 shapes for the edge cases: ragged document tails, one-token and one-block
-documents, top-k covering every block (dense limit), k = 1, and G = 1 / 2 / 8.
+documents, top-k covering every block (dense limit), k = 1, G = 1 / 2 / 8, and
+block patterns (always-kept windows, with and without dilation).
 """
 import numpy as np
 import pytest
@@ -15,19 +16,19 @@ from parity import KL_RTOL, assert_close, check_selection_row
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, inp_cpu):
+def _run(w, inp_cpu, **pattern):
     from block_sparse_attention_proxy_gb300 import msa_get_device_status
     from block_sparse_attention_proxy_gb300.step import params_for, run_step
 
     dev = {k: v.cuda() for k, v in inp_cpu.items()}
-    prm = params_for(inp_cpu["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k)
+    prm = params_for(inp_cpu["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k, **pattern)
     out = run_step(prm, dev)
     assert msa_get_device_status() == 0
     return {k: v.cpu() for k, v in out.items()}
 
 
-def _check_all(w, inp, g):
-    prm = OracleParams(w.hq, w.hkv, w.d, w.dp, w.top_k)
+def _check_all(w, inp, g, window=0, dilation=1):
+    prm = OracleParams(w.hq, w.hkv, w.d, w.dp, w.top_k, window=window, dilation=dilation)
     ref = msa_reference(inp, prm, sel_override=g["sel_idx"], arg_override=g["sel_arg"])
     sel = g["sel_idx"].numpy()
     own = ref["own_sel_idx"]
@@ -41,7 +42,7 @@ def _check_all(w, inp, g):
         for i in range(b - a):
             for gg in range(w.hkv):
                 ties += check_selection_row(sel[a + i, gg], own[a + i, gg], S[i, gg], i // 128,
-                                            w.top_k)
+                                            w.top_k, window, dilation)
     # where the selections agree, the argmax key agrees unless within the tie band
     same = (sel == own).all(-1)
     arg_g = g["sel_arg"].numpy().astype(np.int64)
@@ -100,6 +101,35 @@ def test_edge_shapes(case):
     inp = synth.make_inputs(w)
     g = _run(w, inp)
     _check_all(w, inp, g)
+
+
+PATTERNS = [
+    # (doc lengths, hq, hkv, d, dp, k, structured, window, dilation)
+    ([1, 129, 300, 128, 77, 513, 1500], 8, 2, 128, 64, 6, False, 2, 1),  # ragged, local window
+    ([2048, 700], 8, 4, 128, 64, 5, True, 4, 1),     # window = k-1: sliding window of k blocks
+    ([3000], 4, 1, 64, 32, 8, False, 3, 3),          # dilated window
+    ([1800, 900], 8, 2, 128, 64, 16, True, 5, 2),    # k = 16, dilated, reaching past doc starts
+    ([2500, 260], 4, 2, 128, 64, 4, False, 1, 40),   # dilation beyond the document: no block kept
+]
+
+
+@pytest.mark.parametrize("case", PATTERNS, ids=[f"pattern{i}" for i in range(len(PATTERNS))])
+def test_block_pattern(case):
+    """Always-kept window of w blocks spaced s apart inside the k slots."""
+    lens, hq, hkv, d, dp, k, structured, win, dil = case
+    w = synth.custom(lens, hq, hkv, d, dp, k, seed=300 + len(lens) + k, structured=structured)
+    inp = synth.make_inputs(w)
+    g = _run(w, inp, window=win, dilation=dil)
+    _check_all(w, inp, g, window=win, dilation=dil)
+    if win == k - 1 and dil == 1:  # the selection is the last k blocks, scores aside
+        sel = g["sel_idx"].numpy()
+        cu = inp["cu_seqlens"].tolist()
+        for a, b in zip(cu[:-1], cu[1:]):
+            for i in range(0, b - a, 37):
+                j = i // 128
+                want = list(range(max(0, j - k + 1), j + 1))
+                want += [-1] * (k - len(want))
+                assert (sel[a + i] == np.asarray(want)).all(), (a + i, sel[a + i], want)
 
 
 def test_deterministic():

@@ -37,12 +37,13 @@ def test_noalloc_select_matches_workspace_select_twice():
     import block_sparse_attention_proxy_gb300 as m
     from block_sparse_attention_proxy_gb300.step import params_for
 
-    cases = [synth.custom([700, 1, 1500, 333], 8, 2, 128, 64, 5, seed=41, structured=True),
-             synth.custom([2048], 4, 1, 64, 32, 4, seed=42)]
-    for w in cases:
+    cases = [(synth.custom([700, 1, 1500, 333], 8, 2, 128, 64, 5, seed=41, structured=True), {}),
+             (synth.custom([2048], 4, 1, 64, 32, 4, seed=42), {}),
+             (synth.custom([3000, 500], 8, 2, 128, 64, 6, seed=43), dict(window=3, dilation=2))]
+    for w, pattern in cases:
         inp = synth.make_inputs(w)
         dev = {k: v.cuda() for k, v in inp.items()}
-        prm = params_for(inp["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k)
+        prm = params_for(inp["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k, **pattern)
         ref = _select(m, prm, dev, noalloc=False)
         got = _select(m, prm, dev, noalloc=True)
         for name in ("sel_idx", "sel_arg", "tie"):
