@@ -495,7 +495,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false",
                     help="skip the end-to-end leg (profiling runs only)")
-    ap.add_argument("--cpu-rows", type=int, default=24)
+    ap.add_argument("--cpu-rows", type=int, default=128)
     ap.add_argument("--ref-rows", type=int, default=4)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

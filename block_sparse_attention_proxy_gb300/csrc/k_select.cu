@@ -27,6 +27,7 @@
 // go to slots of their own in shared memory, they never enter the ranked list,
 // and the ranked list fills the other k-1-|window| slots.
 #include <cfloat>
+#include <climits>
 
 #include "msa_internal.cuh"
 
@@ -251,6 +252,11 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     uint32_t dav = 0;
     bool handled_diag = false;
     const float ps = a.proxy_scale;
+    // Always-kept blocks J - dilation * u, u = min(window, J / dilation) .. 1: the
+    // lowest one, then a cursor this warpgroup advances as its blocks (in
+    // increasing order) pass it, so the block loop needs no division.
+    int next_kept = INT_MAX;
+    if (a.window > 0 && J >= a.dilation) next_kept = J - a.dilation * min(a.window, J / a.dilation);
     // Warpgroup e takes the steps m = e, e + 2, ... (its own 256-column
     // accumulator e); each step holds key blocks 2m and 2m + 1.
     bool stop = false;
@@ -269,10 +275,12 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         const bool last = u == 1 || n + 1 >= nblk;
         const uint32_t tb = tbase + lane_off + acc * 256 + u * 128;
         const bool diag = (n == J);
-        // block of the always-kept window (warp-uniform): J - n = dilation * u, 1 <= u <= window
-        const int dj = J - n;
-        const bool forced = a.window > 0 && dj > 0 && dj <= a.window * a.dilation &&
-                            dj % a.dilation == 0;
+        // block of the always-kept window (warp-uniform)
+        bool forced = false;
+        if (!diag && n >= next_kept) {
+          while (next_kept < n) next_kept += a.dilation;
+          forced = n == next_kept;
+        }
         // argmax bookkeeping for every block (ARG), else for the diagonal block only
         const bool track = ARG || diag;  // warp-uniform
         // The 32 scores of the chunk holding the row maximum stay in registers (first chunk
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
           dav = ((uint32_t)n << 8) | (uint32_t)arg;
           handled_diag = true;
         } else if (forced) {  // kept whatever its score: a slot of its own, not the ranking
-          const int u = dj / a.dilation - 1;
+          const int u = (J - n) / a.dilation - 1;
           f_sc[u * 128 + row] = best * ps;
           f_id[u * 128 + row] = ((uint32_t)n << 8) | (uint32_t)arg;
         } else if (need) {
