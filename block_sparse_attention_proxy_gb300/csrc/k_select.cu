@@ -122,7 +122,7 @@ struct SelArgs {
   unsigned* status;
 };
 
-template <int DP, int CAP, bool ARG>
+template <int DP, int CAP, bool ARG, bool WIN>
 __global__ void __launch_bounds__(kSelThreads, 1)
     k_select(const __grid_constant__ CUtensorMap tm_qp, const __grid_constant__ CUtensorMap tm_kp,
              const SelArgs a) {
@@ -137,9 +137,10 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   uint32_t* m_id = reinterpret_cast<uint32_t*>(m_sc + CAP * 128);           // [CAP][128]
   float* d_sc = reinterpret_cast<float*>(m_id + CAP * 128);                 // [128]
   uint32_t* d_id = reinterpret_cast<uint32_t*>(d_sc + 128);                 // [128]
-  float* f_sc = reinterpret_cast<float*>(d_id + 128);          // [CAP][128] always-kept blocks
-  uint32_t* f_id = reinterpret_cast<uint32_t*>(f_sc + CAP * 128);           // [CAP][128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(f_id + CAP * 128);
+  // [CAP][128] always-kept blocks (block pattern only)
+  float* f_sc = reinterpret_cast<float*>(d_id + 128);
+  uint32_t* f_id = reinterpret_cast<uint32_t*>(f_sc + (WIN ? CAP * 128 : 0));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(f_id + (WIN ? CAP * 128 : 0));
   // bars: 0 qfull | 1..S kvfull | S+1..2S kvempty | 2S+1..2S+2 accfull | 2S+3..2S+4 accempty
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kSelStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     // lowest one, then a cursor this warpgroup advances as its blocks (in
     // increasing order) pass it, so the block loop needs no division.
     int next_kept = INT_MAX;
-    if (a.window > 0 && J >= a.dilation) next_kept = J - a.dilation * min(a.window, J / a.dilation);
+    if (WIN && J >= a.dilation) next_kept = J - a.dilation * min(a.window, J / a.dilation);
     // Warpgroup e takes the steps m = e, e + 2, ... (its own 256-column
     // accumulator e); each step holds key blocks 2m and 2m + 1.
     bool stop = false;
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         const bool diag = (n == J);
         // block of the always-kept window (warp-uniform)
         bool forced = false;
-        if (!diag && n >= next_kept) {
+        if (WIN && !diag && n >= next_kept) {
           while (next_kept < n) next_kept += a.dilation;
           forced = n == next_kept;
         }
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       dav = d_id[row];
       const int K = a.K;
       const int nsel = min(J, K - 1);  // off-diagonal blocks kept
-      const int nf = a.window > 0 ? min(a.window, J / a.dilation) : 0;  // always kept
+      const int nf = WIN ? min(a.window, J / a.dilation) : 0;  // always kept
       const int ntop = nsel - nf;      // chosen by score from the other earlier blocks
       uint8_t tie = 0;
       if (J > K - 1 && ntop >= 1) {  // a choice was made: last taken vs first left
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       // the always-kept blocks take list entries ntop .. nsel-1
 #pragma unroll
       for (int i = 0; i < CAP; ++i) {
-        if (i >= ntop && i < nsel) {
+        if (WIN && i >= ntop && i < nsel) {
           sc[i] = f_sc[(i - ntop) * 128 + row];
           id[i] = f_id[(i - ntop) * 128 + row];
         }
@@ -456,25 +457,30 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   }
 }
 
-template <int DP, int CAP, bool ARG>
+template <int DP, int CAP, bool ARG, bool WIN>
 cudaError_t launch_sel_t(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
                          const SelArgs& a, cudaStream_t st) {
   using C = SelCfg<DP>;
-  const size_t smem = 1024 + (1 + 2 * kSelStages) * C::kTileBytes + 2 * CAP * 128 * 8 +
+  const size_t smem = 1024 + (1 + 2 * kSelStages) * C::kTileBytes + (WIN ? 2 : 1) * CAP * 128 * 8 +
                       128 * 8 + (2 * kSelStages + 5) * 8 + 16;
-  cudaError_t e = cudaFuncSetAttribute(k_select<DP, CAP, ARG>,
+  cudaError_t e = cudaFuncSetAttribute(k_select<DP, CAP, ARG, WIN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = s.nb_bound * s.hkv;
-  k_select<DP, CAP, ARG><<<grid, kSelThreads, smem, st>>>(mq, mk, a);
+  k_select<DP, CAP, ARG, WIN><<<grid, kSelThreads, smem, st>>>(mq, mk, a);
   return cudaGetLastError();
 }
 
+// The block pattern is a template switch: without it the block loop and the
+// merge compile exactly as the plain rule needs.
 template <int DP, int CAP>
 cudaError_t launch_sel_a(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
                          const SelArgs& a, bool with_arg, cudaStream_t st) {
-  return with_arg ? launch_sel_t<DP, CAP, true>(s, mq, mk, a, st)
-                  : launch_sel_t<DP, CAP, false>(s, mq, mk, a, st);
+  if (s.window > 0)
+    return with_arg ? launch_sel_t<DP, CAP, true, true>(s, mq, mk, a, st)
+                    : launch_sel_t<DP, CAP, false, true>(s, mq, mk, a, st);
+  return with_arg ? launch_sel_t<DP, CAP, true, false>(s, mq, mk, a, st)
+                  : launch_sel_t<DP, CAP, false, false>(s, mq, mk, a, st);
 }
 
 }  // namespace

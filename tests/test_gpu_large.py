@@ -28,14 +28,17 @@ def _host_inputs(inp):
     return cpu
 
 
-@pytest.mark.parametrize("name", ["128k", "512k", "1m"])
-def test_full_size_sampled(name):
+@pytest.mark.parametrize("name,window,dilation",
+                         [("128k", 0, 1), ("512k", 0, 1), ("1m", 0, 1), ("128k", 5, 3)],
+                         ids=["128k", "512k", "1m", "128k-window5-dilation3"])
+def test_full_size_sampled(name, window, dilation):
     import block_sparse_attention_proxy_gb300 as m
     from block_sparse_attention_proxy_gb300.step import MSAStep, params_for
 
     w = synth.workload(name)
     inp = synth.make_inputs(w, device="cuda")
-    prm_c = params_for(inp["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k)
+    prm_c = params_for(inp["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k,
+                       window=window, dilation=dilation)
     step = MSAStep(prm_c)
     step(inp)
     torch.cuda.synchronize()
@@ -44,7 +47,7 @@ def test_full_size_sampled(name):
     cpu = _host_inputs(inp)
     del inp, step
     torch.cuda.empty_cache()
-    prm = OracleParams(w.hq, w.hkv, w.d, w.dp, w.top_k)
+    prm = OracleParams(w.hq, w.hkv, w.d, w.dp, w.top_k, window=window, dilation=dilation)
     T = w.total_tokens
     sel = g["sel_idx"].numpy()
     arg = g["sel_arg"].numpy()
@@ -55,7 +58,8 @@ def test_full_size_sampled(name):
     for t in rows:
         r = row_reference(cpu, prm, t, sel_override=sel[t], arg_override=arg[t])
         for gg in range(w.hkv):
-            check_selection_row(sel[t, gg], r["sel"][gg], r["pooled"][gg], t // 128, w.top_k)
+            check_selection_row(sel[t, gg], r["sel"][gg], r["pooled"][gg], t // 128, w.top_k,
+                                window, dilation)
         acc["o"][0].append(g["o"][t].float().numpy()); acc["o"][1].append(r["o"])
         acc["lse"][0].append(g["lse"][t].numpy()); acc["lse"][1].append(r["lse"])
         acc["mass"][0].append(g["mass"][t].numpy()); acc["mass"][1].append(r["mass"])
