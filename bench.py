@@ -15,6 +15,9 @@ Prints one JSON line (rank 0).  `value` is the effective TFLOP/s of the step:
 measured step time; proxy scoring is not counted but its time is.  Inputs are
 synthetic (seeded, see synth/) and resident in HBM when the timed region
 starts; they are larger than L2, so no flush is needed between steps.
+`e2e` is the same metric with the inputs in pinned host memory, copied to the
+device every step inside the timed region (HostInputStep: the copies overlap
+the kernels on a copy stream), and the step's loss read back to the host.
 With N > 1 (torchrun), every rank runs an independent replica on its own GPU
 (the path has no exchange step); the aggregate counts all ranks' work over the
 slowest rank's time.
@@ -394,26 +397,24 @@ def run_ours(args):
 
 
 def run_e2e(w, inp, step, fl, K, W, world) -> dict:
-    """The same metric end to end through the C ABI: every step copies its
-    inputs from pinned host memory to the device and reads the step's result,
-    the proxy-KL loss, back to the host, all inside the timed region and in
-    order on one stream (no overlap of copies with compute).  The gradients
-    stay on the device, where a training step consumes them."""
+    """The same metric end to end through the library's host-input API
+    (HostInputStep): every step copies its inputs from pinned host memory to
+    the device and reads the step's result, the proxy-KL loss, back to pinned
+    host memory, all inside the timed region.  The copies run on a copy stream
+    and overlap the kernels (of the same step, for inputs a later call needs,
+    and of the previous step, through two alternating device buffer sets).
+    The gradients stay on the device, where a training step consumes them."""
+    from block_sparse_attention_proxy_gb300.step import HostInputStep
+
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     names_in = ("q", "k", "v", "q_p", "k_p", "dO", "cu_seqlens")
     host_in = {n: inp[n].to("cpu").pin_memory() for n in names_in}
-    names_out = ("kl_loss",)
-    host_out = {n: torch.empty_like(step.out[n], device="cpu").pin_memory() for n in names_out}
-    dev_in = {n: torch.empty_like(inp[n]) for n in names_in}
+    hs = HostInputStep(step.params, inp, step=step)
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    d2h = hs.loss.numel() * hs.loss.element_size()
 
     def e2e_step():
-        for n in names_in:
-            dev_in[n].copy_(host_in[n], non_blocking=True)
-        step(dev_in)
-        for n in names_out:
-            host_out[n].copy_(step.out[n], non_blocking=True)
+        hs(host_in)
 
     for _ in range(max(1, W)):
         e2e_step()
@@ -421,9 +422,10 @@ def run_e2e(w, inp, step, fl, K, W, world) -> dict:
     barrier(world)
     e0, e1 = E(), E()
     e0.record()
+    hs.copy_stream.wait_event(e0)  # no copy of the timed steps starts before e0
     for _ in range(K):
         e2e_step()
-    e1.record()
+    e1.record()  # after the last step's kernels, which wait for all its copies
     torch.cuda.synchronize()
     barrier(world)
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / K, world)

@@ -68,6 +68,64 @@ class MSAStep:
         return self.out
 
 
+class HostInputStep:
+    """Training steps whose inputs arrive in pinned host memory.
+
+    The host-to-device copies run on a copy stream in the order the calls need
+    them (cu_seqlens, q_p, k_p for the selection; k, v, q for the forward; dO
+    for the backward), and each call waits only for its own inputs, so the
+    copies of the later inputs overlap the earlier kernels.  Two sets of device
+    input buffers alternate between steps: the copies of step i also overlap
+    the kernels of step i-1, and wait only for step i-2's kernels, the last to
+    read the set they overwrite.  Each step's proxy-KL loss is copied back to
+    pinned host memory on the compute stream; read it after synchronising.
+    """
+
+    GROUPS = (("cu_seqlens", "q_p", "k_p"), ("k", "v", "q"), ("dO",))
+
+    def __init__(self, params, like: dict, device="cuda", step: MSAStep | None = None):
+        """like: tensors with the shapes and dtypes of one step's inputs; step:
+        an MSAStep of these params whose outputs and workspace to use."""
+        self.step = step if step is not None else MSAStep(params, device)
+        names = [n for grp in self.GROUPS for n in grp]
+        self.bufs = [{n: torch.empty(like[n].shape, dtype=like[n].dtype, device=device)
+                      for n in names} for _ in range(2)]
+        self.done = [None, None]  # kernels of the last step that read buffer set b
+        self.copy_stream = torch.cuda.Stream(device)
+        self.loss = torch.empty(1, dtype=torch.float64).pin_memory()
+        self._n = 0
+
+    def __call__(self, host_inp: dict, loss_out: torch.Tensor | None = None) -> dict:
+        """Queue one step on the current stream; returns the device outputs
+        (valid until the next step's kernels overwrite them)."""
+        b = self._n & 1
+        self._n += 1
+        dev, cs = self.bufs[b], self.copy_stream
+        st = torch.cuda.current_stream(cs.device)
+        if self.done[b] is not None:
+            cs.wait_event(self.done[b])
+        ready = []
+        with torch.cuda.stream(cs):
+            for grp in self.GROUPS:
+                for n in grp:
+                    dev[n].copy_(host_inp[n], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs)
+                ready.append(ev)
+        st.wait_event(ready[0])
+        self.step.select(dev, st)
+        st.wait_event(ready[1])
+        self.step.forward(dev, st)
+        st.wait_event(ready[2])
+        self.step.backward(dev, st)
+        (self.loss if loss_out is None else loss_out).copy_(self.step.out["kl_loss"],
+                                                            non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(st)
+        self.done[b] = done
+        return self.step.out
+
+
 def run_step(params, inp, device="cuda") -> dict:
     step = MSAStep(params, device)
     out = step(inp)

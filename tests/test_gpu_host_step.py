@@ -1,0 +1,45 @@
+"""HostInputStep: inputs in pinned host memory, copied on a copy stream that
+overlaps the kernels (within a step, and across steps through two alternating
+device buffer sets).  Steps queued back to back, with no synchronisation in
+between, must return bit for bit what MSAStep returns on device inputs; the
+fourth step reuses the first buffer set, so a copy that overtook the kernels
+still reading that set would show."""
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+SHAPE = ([2500, 700, 1300], 8, 2, 128, 64, 5)
+
+
+def test_host_input_steps_match_device_steps():
+    from block_sparse_attention_proxy_gb300 import msa_get_device_status
+    from block_sparse_attention_proxy_gb300.step import HostInputStep, MSAStep, params_for
+
+    lens, hq, hkv, d, dp, k = SHAPE
+    sets = [synth.make_inputs(synth.custom(lens, hq, hkv, d, dp, k, seed=60 + i, structured=True))
+            for i in range(3)]
+    prm = params_for(sets[0]["cu_seqlens"].tolist(), hq, hkv, d, dp, k)
+
+    ref = []
+    st = MSAStep(prm)
+    for inp in sets:
+        out = st({n: v.cuda() for n, v in inp.items()})
+        torch.cuda.synchronize()
+        ref.append({n: v.clone() for n, v in out.items()})
+    assert msa_get_device_status() == 0
+
+    host = [{n: v.pin_memory() for n, v in inp.items()} for inp in sets]
+    hs = HostInputStep(prm, sets[0])
+    order = [0, 1, 2, 0]
+    losses = [torch.empty(1, dtype=torch.float64).pin_memory() for _ in order]
+    for j, i in enumerate(order):
+        out = hs(host[i], loss_out=losses[j])
+    torch.cuda.synchronize()
+    assert msa_get_device_status() == 0
+    for j, i in enumerate(order):
+        assert torch.equal(losses[j], ref[i]["kl_loss"].cpu()), (j, i)
+    for n in ("o", "lse", "dq", "dk", "dv", "dq_p", "dk_p", "sel_idx"):
+        assert torch.equal(out[n], ref[order[-1]][n]), n
