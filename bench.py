@@ -189,9 +189,12 @@ def dist_setup():
     if world > 1:
         import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:  # host-only runs of the rank logic (CPU tests)
+            dist.init_process_group("gloo")
+    elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
 
@@ -204,11 +207,14 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time: the aggregate throughput divides every rank's
+    units by it."""
     if world == 1:
         return x
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

@@ -1,0 +1,68 @@
+"""The bench's multi-rank host logic with two gloo ranks on CPU.
+
+The path does not shard across GPUs by exchange: under torchrun every rank
+runs an independent replica, with a barrier on both sides of the timed region
+and the slowest rank's time as the denominator of the aggregate.  These tests
+run that logic, and the launch of the reference arm (rank 0 alone works and
+prints), without a GPU.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+
+    w, r, _ = bench.dist_setup()
+    bench.barrier(w)
+    slowest = bench.max_over_ranks(1.5 + r, w)  # rank r "took" 1.5 + r ms
+    bench.barrier(w)
+    out.put((r, w, dist.get_backend(), slowest))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(60)
+    assert [p.exitcode for p in procs] == [0, 0]
+    assert got == [(0, 2, "gloo", 2.5), (1, 2, "gloo", 2.5)]
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank0():
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl",
+           "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--workload", "tiny",
+           "--ref-rows", "2"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
