@@ -435,9 +435,20 @@ def run_e2e(w, inp, step, fl, K, W, world) -> dict:
     torch.cuda.synchronize()
     barrier(world)
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / K, world)
+    # the host-to-device copy rate alone (one step's inputs, nothing else
+    # running), for reading the number above: the copies hide behind the
+    # kernels while they take less than a step
+    c0, c1 = E(), E()
+    c0.record(hs.copy_stream)
+    with torch.cuda.stream(hs.copy_stream):
+        for n in names_in:
+            hs.bufs[0][n].copy_(host_in[n], non_blocking=True)
+    c1.record(hs.copy_stream)
+    torch.cuda.synchronize()
     return dict(value=round(fl * world / ms_e2e / 1e9, 3), unit=UNIT,
                ms_per_step=round(ms_e2e, 3), h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-               tokens_per_s=round(w.total_tokens * world / ms_e2e * 1e3, 1))
+               tokens_per_s=round(w.total_tokens * world / ms_e2e * 1e3, 1),
+               h2d_gb_per_s_alone=round(h2d / (c0.elapsed_time(c1) * 1e6), 1))
 
 
 
