@@ -98,6 +98,12 @@ class HostInputStep:
     def __call__(self, host_inp: dict, loss_out: torch.Tensor | None = None) -> dict:
         """Queue one step on the current stream; returns the device outputs
         (valid until the next step's kernels overwrite them)."""
+        for grp in self.GROUPS:
+            for n in grp:
+                t = host_inp[n]
+                if t.is_cuda or not t.is_pinned():
+                    raise ValueError(f"HostInputStep: input {n!r} must be a pinned host tensor "
+                                     "(pageable memory would make every copy synchronous)")
         b = self._n & 1
         self._n += 1
         dev, cs = self.bufs[b], self.copy_stream

@@ -43,3 +43,13 @@ def test_host_input_steps_match_device_steps():
         assert torch.equal(losses[j], ref[i]["kl_loss"].cpu()), (j, i)
     for n in ("o", "lse", "dq", "dk", "dv", "dq_p", "dk_p", "sel_idx"):
         assert torch.equal(out[n], ref[order[-1]][n]), n
+
+
+def test_host_input_step_rejects_pageable_inputs():
+    from block_sparse_attention_proxy_gb300.step import HostInputStep, params_for
+
+    lens, hq, hkv, d, dp, k = SHAPE
+    inp = synth.make_inputs(synth.custom(lens, hq, hkv, d, dp, k, seed=60))
+    hs = HostInputStep(params_for(inp["cu_seqlens"].tolist(), hq, hkv, d, dp, k), inp)
+    with pytest.raises(ValueError):
+        hs(inp)  # pageable CPU tensors
