@@ -1,8 +1,8 @@
 """GPU (CUDA path through the C ABI) against the fp64 CPU oracle, every row.
 
 Workloads: the 1024-token tiny step, the 32768-token varlen batch, and small
-shapes for the edge cases: ragged document tails, one-token and one-block
-documents, top-k covering every block (dense limit), k = 1, G = 1 / 2 / 8, and
+shapes for the edge cases: ragged document tails, one-token, one-block and
+empty documents, top-k covering every block (dense limit), k = 1, G = 1 / 2 / 8, and
 block patterns (always-kept windows, with and without dilation).
 """
 import numpy as np
@@ -91,6 +91,7 @@ EDGE = [
     ([400, 1], 4, 2, 128, 64, 1, False),                       # k = 1: diagonal only
     ([2048], 8, 4, 128, 64, 4, True),                          # G = 2, structured keys
     ([1280, 1024], 4, 1, 64, 64, 6, True),                     # d = 64, dp = 64
+    ([0, 300, 0, 0, 700, 0], 4, 2, 64, 32, 3, False),          # empty documents, first and last
 ]
 
 
