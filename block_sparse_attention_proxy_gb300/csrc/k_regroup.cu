@@ -220,35 +220,47 @@ __global__ void __launch_bounds__(32) k_rg_scatter(const int32_t* __restrict__ c
   __syncwarp();
   int d = doc_of_token(cu, ndoc, t0);
   int dstart = cu[d], dend = cu[d + 1], gbd = cu_blocks[d];
-  for (int t = t0; t < t1; ++t) {
-    while (t >= dend && d + 1 < ndoc) {
-      ++d;
-      dstart = dend;
-      dend = cu[d + 1];
-      gbd = cu_blocks[d];
+  // The selection rows of kAhead tokens are loaded together (independent
+  // loads in flight), then the tokens are scattered one by one in order.
+  constexpr int kAhead = 16;
+  for (int tb = t0; tb < t1; tb += kAhead) {
+    int bq[kAhead];
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const int t = tb + u;
+      bq[u] = (t < t1 && lane < K) ? __ldg(sel_idx + ((size_t)t * Hkv + g) * K + lane) : -1;
     }
-    const int j = (t - dstart) / kBlock;
-    const int sd = min(j, K - 1);
-    const int32_t* row = sel_idx + ((size_t)t * Hkv + g) * K;
-    const int b = lane < K ? row[lane] : -1;
-    // identical structural check to row_ok_serial, done across lanes
-    const int prev = __shfl_up_sync(0xffffffffu, b, 1);
-    bool ok = true;
-    if (lane < K) {
-      if (lane < sd) ok = b >= 0 && b < j && (lane == 0 || b > prev);
-      else if (lane == sd) ok = b == j;
-      else ok = b == -1;
-    }
-    if (!__all_sync(0xffffffffu, ok)) continue;
-    if (lane < sd) {
-      const int gbi = gbd + b - lo;
-      if (gbi >= 0 && gbi < R) {
-        const uint32_t pos = off_s[gbi];
-        off_s[gbi] = pos + 1;
-        ent[pos] = ((uint32_t)t << 4) | (uint32_t)lane;
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const int t = tb + u;
+      if (t >= t1) break;  // warp-uniform
+      while (t >= dend && d + 1 < ndoc) {
+        ++d;
+        dstart = dend;
+        dend = cu[d + 1];
+        gbd = cu_blocks[d];
       }
+      const int j = (t - dstart) / kBlock;
+      const int sd = min(j, K - 1);
+      const int b = bq[u];
+      // identical structural check to row_ok_serial, done across lanes
+      const int prev = __shfl_up_sync(0xffffffffu, b, 1);
+      bool ok = true;
+      if (lane < K) {
+        if (lane < sd) ok = b >= 0 && b < j && (lane == 0 || b > prev);
+        else if (lane == sd) ok = b == j;
+        else ok = b == -1;
+      }
+      if (__all_sync(0xffffffffu, ok) && lane < sd) {
+        const int gbi = gbd + b - lo;
+        if (gbi >= 0 && gbi < R) {
+          const uint32_t pos = off_s[gbi];
+          off_s[gbi] = pos + 1;
+          ent[pos] = ((uint32_t)t << 4) | (uint32_t)lane;
+        }
+      }
+      __syncwarp();
     }
-    __syncwarp();
   }
 }
 
