@@ -79,6 +79,8 @@ class HostInputStep:
     the kernels of step i-1, and wait only for step i-2's kernels, the last to
     read the set they overwrite.  Each step's proxy-KL loss is copied back to
     pinned host memory on the compute stream; read it after synchronising.
+    The host tensors are read asynchronously: leave them unchanged until the
+    step's kernels have finished (for instance, until its loss has been read).
     """
 
     GROUPS = (("cu_seqlens", "q_p", "k_p"), ("k", "v", "q"), ("dO",))
