@@ -234,8 +234,12 @@ uint64_t msa_launch_count(void);
  * `start` on the call's stream right before it and `stop` right after it
  * (`start`/`stop` are cudaEvent_t handles owned by the caller; pass null to
  * clear).  which: 1 proxy scoring + selection kernel, 2 forward block kernel,
- * 3 backward block kernel.  Process-global; not for concurrent use from
- * several threads.  Returns MSA_ERR_INVALID_ARG for an unknown `which`.
+ * 3 backward block kernel.  A batch of more than 2048 KV blocks runs the
+ * forward and backward block kernels once per query chunk; `start` is then
+ * recorded before the first of them and `stop` after the last, so the span
+ * includes the merge / reduce passes of the earlier chunks in between.
+ * Process-global; not for concurrent use from several threads.  Returns
+ * MSA_ERR_INVALID_ARG for an unknown `which`.
  */
 typedef struct CUevent_st* msa_event_t;
 msa_status msa_set_profile_events(int which, msa_event_t start, msa_event_t stop);
