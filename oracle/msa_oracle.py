@@ -49,8 +49,10 @@ listed as a reading in the design notes):
 
 Every function below is pinned by tests that do not reuse its code: dense
 causal attention when k covers every block, brute-force subset search for the
-selection, central finite differences and torch.autograd for the gradients,
-and the invariants sum p = sum m = 1, sum g = 0, KL >= 0.
+selection (with and without an always-kept window), sliding-window attention
+through torch's SDPA with an explicit mask when the window fills the k slots,
+central finite differences and torch.autograd for the gradients, and the
+invariants sum p = sum m = 1, sum g = 0, KL >= 0.
 """
 from __future__ import annotations
 
