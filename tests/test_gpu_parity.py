@@ -111,6 +111,7 @@ PATTERNS = [
     ([3000], 4, 1, 64, 32, 8, False, 3, 3),          # dilated window
     ([1800, 900], 8, 2, 128, 64, 16, True, 5, 2),    # k = 16, dilated, reaching past doc starts
     ([2500, 260], 4, 2, 128, 64, 4, False, 1, 40),   # dilation beyond the document: no block kept
+    ([3200, 900], 8, 2, 128, 64, 4, True, 3, 3),     # every earlier slot kept once j >= 9: no ranking
 ]
 
 
@@ -240,17 +241,18 @@ def test_device_check_on_malformed_inputs():
     assert m.msa_get_device_status() == 6
 
 
-def test_query_chunks_match_oracle_and_single_pass(monkeypatch):
+@pytest.mark.parametrize("pattern", [{}, dict(window=2, dilation=2)], ids=["plain", "window"])
+def test_query_chunks_match_oracle_and_single_pass(monkeypatch, pattern):
     """The slot partials processed in query chunks of 3 KV blocks (9 chunks with
     boundaries inside documents) agree with the oracle, and with one pass:
     row-local outputs bit for bit, the block sums dK/dV/dk_p to rounding."""
     w = synth.custom([700, 1100, 300, 900], 8, 2, 128, 64, 4, seed=7, structured=True)
     inp = synth.make_inputs(w)
     monkeypatch.setenv("MSA_QUERY_CHUNK_BLOCKS", "3")
-    g = _run(w, inp)
-    _check_all(w, inp, g)
+    g = _run(w, inp, **pattern)
+    _check_all(w, inp, g, **pattern)
     monkeypatch.delenv("MSA_QUERY_CHUNK_BLOCKS")
-    one = _run(w, inp)
+    one = _run(w, inp, **pattern)
     for n in ("sel_idx", "sel_arg", "o", "o_res", "lse", "mass", "dq", "dq_p"):
         assert torch.equal(g[n], one[n]), n
     for n in ("dk", "dv", "dk_p"):
