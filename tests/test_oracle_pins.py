@@ -332,10 +332,16 @@ def test_invariants():
             np.testing.assert_allclose(ref["dv"][a:b, g].sum(0), dO[a:b, g * G:(g + 1) * G].sum((0, 1)),
                                        atol=1e-10)
             np.testing.assert_allclose(ref["dk"][a:b, g].sum(0), 0.0, atol=1e-10)
-    # effective pair count equals the mask size enumerated by the reference
-    assert mask_pair_count(inp["cu_seqlens"], prm) == int(
-        sum(min(i // block, k - 1) * block + i % block + 1
-            for a, b in zip(cu[:-1], cu[1:]) for i in range(b - a))) * hq
+    # the effective pair count equals the mask size counted key by key from the
+    # selection the reference attended over (every selected block, keys <= i)
+    sel = ref["sel_idx"]
+    counted = 0
+    for a, b in zip(cu[:-1], cu[1:]):
+        for i in range(b - a):
+            for blk in sel[a + i, 0]:
+                if blk >= 0:
+                    counted += sum(1 for key in range(blk * block, (blk + 1) * block) if key <= i)
+    assert mask_pair_count(inp["cu_seqlens"], prm) == counted * hq
 
 
 def test_uniform_scores_closed_form():
