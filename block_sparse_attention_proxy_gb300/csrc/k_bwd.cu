@@ -24,12 +24,13 @@
 // entry (token, slot, argmax, g_b, and LSE and D of the token's G heads)
 // contiguously in the list's order, so a tile's metadata is one bulk copy.
 //
-// Roles (320 threads): warps 0-7 epilogue (two warpgroups, each half of a
-// tile's rows), warp 8 TMA producer, warp 9 MMA issuer.  Two tiles are in
-// flight: TMEM holds two slots of {S^T, dP^T}; after the epilogue has read a
-// slot it writes P^T (bf16) back into the slot's dP^T columns, where the dV
-// product reads it as its A operand, and the slot's S^T columns receive that
-// tile's dQ^T.  dS^T has one shared-memory buffer: a tile's first dS^T
+// Roles (512 threads): warps 0-7 softmax epilogue (two warpgroups, each half
+// of a tile's rows), warps 8-11 dQ drain, warp 12 producer (Q/dO gathers by
+// cp.async, records and q_p rows by bulk/TMA copies), warp 13 MMA issuer,
+// warps 14-15 idle.  Two tiles are in flight: TMEM holds two slots of
+// {S^T, dP^T}; after the epilogue has read a slot it writes P^T (bf16) back
+// into the slot's dP^T columns, where the dV product reads it as its A
+// operand, and the slot's S^T columns receive that tile's dQ^T.  dS^T has one shared-memory buffer: a tile's first dS^T
 // store waits for the previous tile's products.  The MMA warp issues
 // S^T/dP^T of tile n+1 ahead of the dV/dK/dQ products of tile n, so the
 // epilogue of one tile runs while the tensor core works on its neighbours.

@@ -83,7 +83,15 @@
  *     no CPU fallback.
  *   - Errors found on the device (malformed cu_seqlens, an internal wait that
  *     ran out) are recorded in a device status word; read it with
- *     msa_get_device_status after the stream has reached the call.
+ *     msa_get_device_status after the stream has reached the call.  Its
+ *     address is looked up once per device and cached for the life of the
+ *     process, so the library must not be used after cudaDeviceReset.
+ *   - Batches of more than 2048 KV blocks run the forward and backward block
+ *     kernels in query chunks of 2048 blocks (this bounds the workspace).  The
+ *     environment variable MSA_QUERY_CHUNK_BLOCKS, read at every call, sets a
+ *     smaller positive chunk (in KV blocks) instead; it exists so that tests
+ *     can take the chunked path on small batches, and results do not depend
+ *     on it beyond fp32 rounding of dk, dv and dk_p (summed chunk by chunk).
  */
 #ifndef MSA_H_
 #define MSA_H_
@@ -122,8 +130,10 @@ typedef struct msa_params {
  * since.  The call then reuses the block lists (queries regrouped per KV
  * block) left at the front of the workspace instead of rebuilding them (5
  * fewer kernel launches).  All three workspace layouts share that prefix.
- * msa_proxy_select ignores the flag.  If the condition does not hold, the
- * results are undefined.
+ * msa_proxy_select ignores the flag.  msa_proxy_select_noalloc has no
+ * workspace and builds no block lists, so the flag must not be set on a call
+ * whose preceding call was msa_proxy_select_noalloc.  If the condition does
+ * not hold, the results are undefined.
  */
 #define MSA_FLAG_REUSE_REGROUP 0x1u
 
@@ -198,7 +208,13 @@ msa_status msa_bwd(const msa_params* params, const int32_t* cu_seqlens, const ui
  *     call before any stream capture;
  *   - all calls share the one array: calls that overlap on the GPU (for
  *     example on two streams without ordering between them) race on it.
- *     Each call writes every entry it reads, so no clearing is needed.
+ *     Each call writes every entry it reads, so no clearing is needed;
+ *   - it leaves no block lists anywhere, so a following msa_fwd or msa_bwd
+ *     must not set MSA_FLAG_REUSE_REGROUP (it builds its own lists instead);
+ *   - the array's address is cached per device for the life of the process:
+ *     after cudaDeviceReset (or any teardown of the device's primary context)
+ *     the library must not be called again in that process.  The same holds
+ *     for the device status word every entry point uses.
  * The pages have no counterpart of this entry point.
  */
 msa_status msa_proxy_select_noalloc(const msa_params* params, const int32_t* cu_seqlens,
