@@ -7,24 +7,31 @@ forward (msa_fwd) and backward with the fused proxy-KL gradient (msa_bwd), all
 through the C ABI of libmsa.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 128k|512k|1m|varlen|tiny]
-                    [--impl ours|reference] [--no-dense] [--no-cpu-baseline]
+                    [--impl ours|reference] [--no-dense] [--no-cpu-baseline] [--no-configs]
 
-Prints one JSON line (rank 0).  `value` is the effective TFLOP/s of the step:
+Prints one JSON line (rank 0).  `value` is the effective TFLOP/s of the step
+on the headline workload (128k tokens unless --workload says otherwise):
 14*d FLOPs per (query head, key) pair inside the selection mask (4d forward,
 10d backward; the diagonal block counts only its causal keys), divided by the
 measured step time; proxy scoring is not counted but its time is.  Inputs are
 synthetic (seeded, see synth/) and resident in HBM when the timed region
 starts; they are larger than L2, so no flush is needed between steps.
 `e2e` is the same metric with the inputs in pinned host memory, copied to the
-device every step inside the timed region (HostInputStep: the copies overlap
-the kernels on a copy stream), and the step's loss read back to the host.
+device every step inside the timed region, and the step's results (O, LSE,
+the five gradients, the loss) copied back to pinned host memory, also inside
+it (HostInputStep: the copies overlap the kernels on two copy streams).
+`per_config` repeats the measurement for every workload of the metric's range
+(1k tiny, 32k varlen, 128k, 512k, 1M), each with the dense SDPA comparator and
+the fp64 CPU oracle timed on the host cores (every row for the tiny and varlen
+workloads, a seeded sample of rows for the others).
 With N > 1 (torchrun), every rank runs an independent replica on its own GPU
 (the path has no exchange step); the aggregate counts all ranks' work over the
-slowest rank's time.
+slowest rank's time; per_config is measured on rank 0's GPU only.
 """
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -219,52 +226,110 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def dense_sdpa(w, inp, steps=2, warmup=1) -> dict:
-    """torch SDPA (library flash/cuDNN backend) causal GQA fwd+bwd at the same shapes."""
-    try:
-        cu = inp["cu_seqlens"].tolist()
-        qs = inp["q"].transpose(0, 1).unsqueeze(0)
-        ks = inp["k"].transpose(0, 1).unsqueeze(0)
-        vs = inp["v"].transpose(0, 1).unsqueeze(0)
-        dos = inp["dO"].transpose(0, 1).unsqueeze(0)
+def config_of(w, world: int = 1) -> dict:
+    """The `config` object of the JSON line (identical in both arms)."""
+    return dict(workload=f"{w.name}: {w.total_tokens} tokens in {w.num_docs} doc(s), "
+                         f"Hq={w.hq} Hkv={w.hkv} d={w.d} dp={w.dp} block={w.block} "
+                         f"top-k={w.top_k}" + (", rank-8 structured k/k_p" if w.structured else ""),
+                tokens=w.total_tokens, l2="inputs larger than L2 (no flush)",
+                parallelism="replicas" if world > 1 else "single GPU")
 
-        def one():
-            for a, b in zip(cu[:-1], cu[1:]):
+
+def make_device_inputs(w) -> dict:
+    """Seeded inputs on the device: drawn on the CPU for the small workloads (so
+    a CPU process can redraw the very same tensors), on the GPU for the rest."""
+    if w.total_tokens <= 65536:
+        return {k: v.cuda() for k, v in synth.make_inputs(w, device="cpu").items()}
+    return synth.make_inputs(w, device="cuda")
+
+
+def dense_sdpa(w, inp, steps=2, warmup=1, warm_tokens=None) -> dict:
+    """torch SDPA (library backend) causal GQA fwd+bwd at the same shapes.
+
+    Backends are tried in order: cuDNN with native GQA, cuDNN with K/V
+    expanded to every query head, torch's flash kernel, then torch's default
+    choice; the first that runs is timed.  warm_tokens: warm up on a prefix of
+    that many tokens instead of the full batch (long sequences)."""
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+
+    cu = inp["cu_seqlens"].tolist()
+    qs = inp["q"].transpose(0, 1).unsqueeze(0)
+    ks = inp["k"].transpose(0, 1).unsqueeze(0)
+    vs = inp["v"].transpose(0, 1).unsqueeze(0)
+    dos = inp["dO"].transpose(0, 1).unsqueeze(0)
+    G = w.hq // w.hkv
+    attempts = ((SDPBackend.CUDNN_ATTENTION, True, "cuDNN, native GQA"),
+                (SDPBackend.CUDNN_ATTENTION, False, "cuDNN, K/V expanded per query head"),
+                (SDPBackend.FLASH_ATTENTION, True, "flash (torch), native GQA"),
+                (None, True, "torch default choice, native GQA"))
+    errors = []
+    for backend, native, label in attempts:
+        def one(limit=None):
+            spans = list(zip(cu[:-1], cu[1:]))
+            if limit is not None:
+                spans = [(spans[0][0], min(spans[0][1], spans[0][0] + limit))]
+            for a, b in spans:
                 q = qs[:, :, a:b].detach().requires_grad_(True)
                 k = ks[:, :, a:b].detach().requires_grad_(True)
                 v = vs[:, :, a:b].detach().requires_grad_(True)
-                o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True,
-                                                                     scale=1.0, enable_gqa=True)
+                kk, vv = (k, v) if native else (k.repeat_interleave(G, 1), v.repeat_interleave(G, 1))
+                o = torch.nn.functional.scaled_dot_product_attention(
+                    q, kk, vv, is_causal=True, scale=1.0, enable_gqa=native and G > 1)
                 o.backward(dos[:, :, a:b])
 
-        for _ in range(warmup):
-            one()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(steps):
-            one()
-        e1.record()
-        torch.cuda.synchronize()
+        try:
+            ctx = sdpa_kernel(backend) if backend is not None else contextlib.nullcontext()
+            with ctx:
+                for _ in range(warmup):
+                    one(warm_tokens)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(steps):
+                    one()
+                e1.record()
+                torch.cuda.synchronize()
+        except Exception as ex:  # the comparator is optional context
+            errors.append(f"{label}: {type(ex).__name__}: {str(ex)[:120]}")
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            continue
         ms = e0.elapsed_time(e1) / steps
         dense_pairs = sum(L * (L + 1) // 2 for L in w.doc_lengths) * w.hq
         fl = 14.0 * w.d * dense_pairs
-        return dict(impl="torch.nn.functional.scaled_dot_product_attention (causal, enable_gqa)",
+        torch.cuda.empty_cache()
+        return dict(impl=f"torch.nn.functional.scaled_dot_product_attention, causal, {label}",
                     ms_per_step=round(ms, 3), tflops=round(fl / ms / 1e9, 2),
-                    tokens_per_s=round(w.total_tokens / ms * 1e3, 1), steps=steps)
-    except Exception as ex:  # the comparator is optional context
-        return dict(unavailable=f"{type(ex).__name__}: {ex}"[:200])
+                    tokens_per_s=round(w.total_tokens / ms * 1e3, 1), steps=steps,
+                    warmup=warmup, warm_tokens=warm_tokens, skipped=errors or None)
+    return dict(unavailable="; ".join(errors)[:400])
+
+
+class _Rows:
+    """Rows t of a [T, ...] device tensor copied to the host (the oracle reads
+    q, dO and q_p only at the sampled rows)."""
+
+    def __init__(self, dev, rows):
+        self.rows = {int(t): dev[int(t)].to("cpu") for t in rows}
+
+    def __getitem__(self, t):
+        return self.rows[int(t)]
 
 
 def cpu_baseline(w, inp, n_rows: int, seed: int) -> dict:
     """The fp64 oracle as it stands, on a seeded sample of query rows (every
     head and group of each row, forward and backward incl. its dK/dV/dk_p
-    contributions), on this host's cores."""
+    contributions), on this host's cores.  The oracle reads the key-side
+    tensors up to each row; those are copied to the host once (k_p upcast to
+    fp64 once, exactly, since every row reads its whole prefix)."""
     from oracle import OracleParams, row_reference
 
     prm = OracleParams(w.hq, w.hkv, w.d, w.dp, w.top_k)
-    cpu = {k: v.detach().to("cpu") for k, v in inp.items()}
     rows = synth.sample_rows(w.total_tokens, n_rows, seed + 1000).tolist()
+    cpu = dict(cu_seqlens=inp["cu_seqlens"].to("cpu"), k=inp["k"].to("cpu"), v=inp["v"].to("cpu"),
+               k_p=inp["k_p"].to("cpu").double().numpy())
+    for n in ("q", "dO", "q_p"):
+        cpu[n] = _Rows(inp[n], rows)
     cu = cpu["cu_seqlens"].tolist()
     t0 = time.perf_counter()
     pairs = 0
@@ -275,30 +340,44 @@ def cpu_baseline(w, inp, n_rows: int, seed: int) -> dict:
         pairs += min(i // 128, w.top_k - 1) * 128 + i % 128 + 1
     dt = time.perf_counter() - t0
     fl = 14.0 * w.d * w.hq * pairs
-    return dict(value=round(fl / dt / 1e12, 6), unit=UNIT, cores=os.cpu_count(), kind="oracle",
+    return dict(value=round(fl / dt / 1e12, 6), unit=UNIT, cores=torch.get_num_threads(),
+                kind="oracle",
                 sample=f"{len(rows)} seeded query rows of the {w.name} workload (all heads and "
                        f"groups, fwd+bwd); {dt:.1f} s wall",
                 seconds=round(dt, 2), tokens_per_s=round(len(rows) / dt, 3))
 
 
-def run_ours(args):
-    import block_sparse_attention_proxy_gb300 as m
-    from block_sparse_attention_proxy_gb300.step import MSAStep, params_for
+def _oracle_all_rows(names, threads, queue):
+    """Child process (spawned): the fp64 oracle on every row of the named small
+    workloads, whose inputs it redraws on the CPU from the same seeds."""
+    torch.set_num_threads(threads)
+    from oracle import OracleParams, msa_reference
 
-    world, rank, local = dist_setup()
-    m.load()
-    w = synth.workload(args.workload)
-    c = work_counts(w)
-    inp = synth.make_inputs(w, device="cuda")
-    prm = params_for(inp["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k)
-    step = MSAStep(prm)
-    K, W = args.steps, args.warmup
+    for name in names:
+        w = synth.workload(name)
+        inp = synth.make_inputs(w, device="cpu")
+        c = work_counts(w)
+        t0 = time.perf_counter()
+        msa_reference(inp, OracleParams(w.hq, w.hkv, w.d, w.dp, w.top_k), with_grads=True)
+        dt = time.perf_counter() - t0
+        fl = flops_effective(w, c)
+        queue.put((name, dict(value=round(fl / dt / 1e12, 6), unit=UNIT, cores=threads,
+                              kind="oracle",
+                              sample=f"every row of the {name} workload ({w.total_tokens} tokens, "
+                                     f"all heads and groups, fwd+bwd); {dt:.1f} s wall",
+                              seconds=round(dt, 2), tokens_per_s=round(w.total_tokens / dt, 3))))
+
+
+def time_steps(step, inp, K, W, world, profile=True):
+    """W untimed steps, then K steps timed with CUDA events between barriers;
+    per-call and per-block-kernel times from events recorded on the stream."""
+    import block_sparse_attention_proxy_gb300 as m
+
     for _ in range(W):
         step(inp)
     torch.cuda.synchronize()
     if m.msa_get_device_status() != 0:
         raise RuntimeError(f"device status {m.msa_last_status_word():#x} after warm-up")
-
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     kev = [[(E(), E()) for _ in range(3)] for _ in range(K)]
     call_ev = [[E() for _ in range(4)] for _ in range(K)]
@@ -315,8 +394,9 @@ def run_ours(args):
     launches0 = m.msa_launch_count()
     t0.record()
     for i in range(K):
-        for kid in range(3):
-            m.msa_set_profile_events(kid + 1, *kev[i][kid])
+        if profile:
+            for kid in range(3):
+                m.msa_set_profile_events(kid + 1, *kev[i][kid])
         call_ev[i][0].record()
         step.select(inp)
         call_ev[i][1].record()
@@ -335,14 +415,93 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status {m.msa_last_status_word():#x} in the timed region")
     ms_local = t0.elapsed_time(t1) / K
-    ms = max_over_ranks(ms_local, world)
-    kern_ms = {kid + 1: sum(kev[i][kid][0].elapsed_time(kev[i][kid][1]) for i in range(K)) / K
-               for kid in range(3)}
+    kern_ms = ({kid + 1: sum(kev[i][kid][0].elapsed_time(kev[i][kid][1]) for i in range(K)) / K
+                for kid in range(3)} if profile else {})
     calls = {n: sum(call_ev[i][a].elapsed_time(call_ev[i][a + 1]) for i in range(K)) / K
              for n, a in (("select", 0), ("fwd", 1), ("bwd", 2))}
+    return ms_local, kern_ms, calls, launches, clk
+
+
+# steps, warm-up, dense-comparator steps, CPU-oracle rows (None: every row, in
+# the spawned process) of the per-config records; the headline workload uses
+# the command line's steps and warm-up
+PER_CONFIG = {"tiny": (10, 3, 5, None), "varlen": (10, 3, 3, None), "128k": (5, 3, 1, 64),
+              "512k": (3, 3, 1, 32), "1m": (3, 3, 1, 24)}
+
+
+def measure_config(name, peaks, args, cpu_rows, dense_steps, K, W, world=1) -> dict:
+    """One workload: step time, kernel split, dense comparator, CPU oracle."""
+    from block_sparse_attention_proxy_gb300.step import MSAStep, params_for
+
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats()
+    w = synth.workload(name)
+    c = work_counts(w)
+    inp = make_device_inputs(w)
+    prm = params_for(inp["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k)
+    step = MSAStep(prm)
+    ms, kern_ms, calls, launches, clk = time_steps(step, inp, K, W, world)
+    fl = flops_effective(w, c)
+    models = kernel_models(w, c)
+    rec = dict(workload=config_of(w)["workload"], tokens=w.total_tokens, steps=K, warmup=W,
+               ms_per_step=round(ms, 3), tflops=round(fl / ms / 1e9, 3),
+               tokens_per_s=round(w.total_tokens / ms * 1e3, 1),
+               frac_of_bf16_peak=round(fl / ms / 1e9 / peaks["bf16_tflops"], 4),
+               work_tflops=round((fl + 2.0 * w.dp * w.hkv * c["causal"]) / ms / 1e9, 3),
+               kernels_ms={models[k]["name"]: round(v, 3) for k, v in kern_ms.items()},
+               calls_ms={k: round(v, 3) for k, v in calls.items()},
+               gpu_launches=int(launches), clocks=clk)
+    del step
+    torch.cuda.empty_cache()
+    rec["device_peak_gb"] = round(torch.cuda.max_memory_allocated() / 1e9, 1)
+    if args.dense:
+        long = w.total_tokens > 200000
+        rec["dense_sdpa"] = dense_sdpa(w, inp, steps=dense_steps, warmup=1,
+                                       warm_tokens=8192 if long else None)
+    if args.cpu_baseline and cpu_rows is not None:
+        rec["cpu_baseline"] = cpu_baseline(w, inp, cpu_rows, w.seed)
+    del inp
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_ours(args):
+    import block_sparse_attention_proxy_gb300 as m
+    from block_sparse_attention_proxy_gb300.step import MSAStep, params_for
+
+    world, rank, local = dist_setup()
+    m.load()
+    peaks = load_peaks()
+    wanted = [n for n in args.configs.split(",") if n] if rank == 0 else []
+    for n in wanted:
+        if n not in PER_CONFIG:
+            raise SystemExit(f"--configs: unknown workload {n!r} (choose from {', '.join(PER_CONFIG)})")
+    configs = [n for n in PER_CONFIG if n in wanted and n != args.workload]
+    # the CPU oracle on every row of the small workloads runs in a spawned
+    # process while this one drives the GPU; the sampled-row baselines of this
+    # process run after it has finished, so the two never share the cores
+    oracle_proc, oracle_q = None, None
+    full_rows = [n for n in configs if PER_CONFIG[n][3] is None]
+    if args.cpu_baseline and full_rows:
+        import multiprocessing as mp
+
+        ctx = mp.get_context("spawn")
+        oracle_q = ctx.Queue()
+        oracle_proc = ctx.Process(target=_oracle_all_rows,
+                                  args=(full_rows, max(1, (os.cpu_count() or 2) - 2), oracle_q),
+                                  daemon=True)
+        oracle_proc.start()
+
+    w = synth.workload(args.workload)
+    c = work_counts(w)
+    inp = make_device_inputs(w)
+    prm = params_for(inp["cu_seqlens"].tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k)
+    step = MSAStep(prm)
+    K, W = args.steps, args.warmup
+    ms_local, kern_ms, calls, launches, clk = time_steps(step, inp, K, W, world)
+    ms = max_over_ranks(ms_local, world)
     fl = flops_effective(w, c)
     value = fl * world / ms / 1e9
-    peaks = load_peaks()
     models = kernel_models(w, c)
     top = max(kern_ms, key=lambda k: kern_ms[k])
     mdl = models[top]
@@ -363,36 +522,64 @@ def run_ours(args):
                                                          (1e9 if models[k]["bound"] == "tensor"
                                                           else 1e6), 2),
                                           unit=models[k]["unit"]) for k in kern_ms}
+    device_peak = round(torch.cuda.max_memory_allocated() / 1e9, 1)
 
     # ---- end to end through the C ABI with host buffers ----
-    e2e = None
-    if args.e2e:
-        e2e = run_e2e(w, inp, step, fl, K, W, world)
-
+    e2e = run_e2e(w, inp, step, fl, K, W, world) if args.e2e else None
+    del step
+    torch.cuda.empty_cache()
     dense = dense_sdpa(w, inp) if (args.dense and rank == 0) else None
+
+    # ---- the other workloads of the metric's range ----
+    per_config = {}
+    for name in configs:
+        Kc, Wc, dsteps, rows = PER_CONFIG[name]
+        try:
+            per_config[name] = measure_config(name, peaks, args, None, dsteps, Kc, Wc)
+        except torch.cuda.OutOfMemoryError as ex:
+            per_config[name] = dict(unavailable=f"out of device memory: {str(ex)[:160]}")
+            torch.cuda.empty_cache()
     cpu = None
+    if oracle_proc is not None:
+        oracle_proc.join()
+        while not oracle_q.empty():
+            name, rec = oracle_q.get()
+            per_config[name]["cpu_baseline"] = rec
     if args.cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(w, inp, args.cpu_rows, w.seed)
+        for name in configs:
+            rows = PER_CONFIG[name][3]
+            if rows is not None and "unavailable" not in per_config[name]:
+                wc = synth.workload(name)
+                ic = make_device_inputs(wc)
+                per_config[name]["cpu_baseline"] = cpu_baseline(wc, ic, rows, wc.seed)
+                del ic
+                torch.cuda.empty_cache()
+    if configs:
+        per_config[w.name] = dict(workload=config_of(w)["workload"], tokens=w.total_tokens,
+                                  steps=K, warmup=W, ms_per_step=round(ms, 3),
+                                  tflops=round(value / world, 3),
+                                  tokens_per_s=round(w.total_tokens / ms * 1e3, 1),
+                                  frac_of_bf16_peak=round(value / world / peaks["bf16_tflops"], 4),
+                                  kernels_ms={k: v["ms"] for k, v in per_kernel.items()},
+                                  calls_ms={k: round(v, 3) for k, v in calls.items()},
+                                  device_peak_gb=device_peak, dense_sdpa=dense,
+                                  cpu_baseline=cpu, note="the headline line's own measurement")
 
     line = dict(
         metric=METRIC, value=round(value, 3), unit=UNIT, n_gpus=world, steps=K, warmup=W,
         ms_per_step=round(ms, 3), higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="bf16", data="synthetic (seeded; see synth/)",
-        config=dict(workload=f"{w.name}: {w.total_tokens} tokens in {w.num_docs} doc(s), "
-                             f"Hq={w.hq} Hkv={w.hkv} d={w.d} dp={w.dp} block={w.block} "
-                             f"top-k={w.top_k}" + (", rank-8 structured k/k_p"
-                                                   if w.structured else ""),
-                    tokens=w.total_tokens, l2="inputs larger than L2 (no flush)",
-                    parallelism="replicas" if world > 1 else "single GPU"),
+        config=config_of(w, world),
         tokens_per_s=round(w.total_tokens * world / ms * 1e3, 1),
         work_tflops=round((fl + 2.0 * w.dp * w.hkv * c["causal"]) * world / ms / 1e9, 3),
         frac_of_bf16_peak=round(value / world / peaks["bf16_tflops"], 4),
         frac_of_bf16_sustained=round(value / world / peaks["bf16_tflops_sustained"], 4),
-        device_peak_gb=round(torch.cuda.max_memory_allocated() / 1e9, 1),
+        device_peak_gb=device_peak,
         roofline=roofline, kernels=per_kernel,
         calls_ms={k: round(v, 3) for k, v in calls.items()},
         cpu_baseline=cpu, e2e=e2e, gpu_launches=int(launches), clocks=clk,
-        dense_sdpa=dense,
+        dense_sdpa=dense, per_config=per_config or None,
     )
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -405,51 +592,62 @@ def run_ours(args):
 def run_e2e(w, inp, step, fl, K, W, world) -> dict:
     """The same metric end to end through the library's host-input API
     (HostInputStep): every step copies its inputs from pinned host memory to
-    the device and reads the step's result, the proxy-KL loss, back to pinned
-    host memory, all inside the timed region.  The copies run on a copy stream
-    and overlap the kernels (of the same step, for inputs a later call needs,
-    and of the previous step, through two alternating device buffer sets).
-    The gradients stay on the device, where a training step consumes them."""
+    the device and its results (O, LSE, the five gradients and the loss) back
+    to pinned host memory, all inside the timed region.  The copies run on two
+    copy streams and overlap the kernels (inputs of later calls and of the next
+    step; O during the backward; the gradients during the next step's
+    selection and forward)."""
     from block_sparse_attention_proxy_gb300.step import HostInputStep
 
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     names_in = ("q", "k", "v", "q_p", "k_p", "dO", "cu_seqlens")
     host_in = {n: inp[n].to("cpu").pin_memory() for n in names_in}
     hs = HostInputStep(step.params, inp, step=step)
+    host_out = hs.allocate_host_outputs()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = hs.loss.numel() * hs.loss.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
     def e2e_step():
-        hs(host_in)
+        hs(host_in, host_out=host_out)
 
     for _ in range(max(1, W)):
         e2e_step()
+    hs.wait_outputs()
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = E(), E()
     e0.record()
     hs.copy_stream.wait_event(e0)  # no copy of the timed steps starts before e0
+    hs.out_stream.wait_event(e0)
     for _ in range(K):
         e2e_step()
-    e1.record()  # after the last step's kernels, which wait for all its copies
+    hs.wait_outputs()  # the last step's results are on the host before e1
+    e1.record()
     torch.cuda.synchronize()
     barrier(world)
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / K, world)
-    # the host-to-device copy rate alone (one step's inputs, nothing else
-    # running), for reading the number above: the copies hide behind the
-    # kernels while they take less than a step
-    c0, c1 = E(), E()
+    # copy rates alone (one step's inputs / results, nothing else running), for
+    # reading the number above: the copies hide behind the kernels while they
+    # take less than a step
+    c0, c1, c2, c3 = E(), E(), E(), E()
     c0.record(hs.copy_stream)
     with torch.cuda.stream(hs.copy_stream):
         for n in names_in:
             hs.bufs[0][n].copy_(host_in[n], non_blocking=True)
     c1.record(hs.copy_stream)
     torch.cuda.synchronize()
+    c2.record(hs.out_stream)
+    with torch.cuda.stream(hs.out_stream):
+        for n, t in host_out.items():
+            t.copy_(step.out[n], non_blocking=True)
+    c3.record(hs.out_stream)
+    torch.cuda.synchronize()
     return dict(value=round(fl * world / ms_e2e / 1e9, 3), unit=UNIT,
-               ms_per_step=round(ms_e2e, 3), h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-               tokens_per_s=round(w.total_tokens * world / ms_e2e * 1e3, 1),
-               h2d_gb_per_s_alone=round(h2d / (c0.elapsed_time(c1) * 1e6), 1))
-
+                ms_per_step=round(ms_e2e, 3), h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                tokens_per_s=round(w.total_tokens * world / ms_e2e * 1e3, 1),
+                returned=list(host_out),
+                h2d_gb_per_s_alone=round(h2d / (c0.elapsed_time(c1) * 1e6), 1),
+                d2h_gb_per_s_alone=round(d2h / (c2.elapsed_time(c3) * 1e6), 1))
 
 
 # ---------------------------------------------------------------------------
@@ -459,6 +657,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     from oracle import OracleParams, row_reference
 
     w = synth.workload(args.workload)
@@ -493,8 +692,7 @@ def run_reference(args):
         metric=METRIC, value=round(value, 6), unit=UNIT, n_gpus=int(os.environ.get("WORLD_SIZE", 1)),
         steps=args.steps, warmup=args.warmup, ms_per_step=round(ms, 3), higher_is_better=True,
         scaling="weak", vs_baseline=None, dtype="f64", data="synthetic (seeded; see synth/)",
-        config=dict(workload=f"{w.name}: {w.total_tokens} tokens, Hq={w.hq} Hkv={w.hkv} d={w.d} "
-                             f"dp={w.dp} top-k={w.top_k}", tokens=w.total_tokens),
+        config=config_of(w, world),
         impl="reference",
         cpu_baseline=dict(kind="oracle", cores=os.cpu_count(), sample=sample, value=round(value, 6),
                           unit=UNIT),
@@ -514,6 +712,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false",
                     help="skip the end-to-end leg (profiling runs only)")
+    ap.add_argument("--configs", default=",".join(PER_CONFIG),
+                    help="comma-separated workloads measured besides the headline one "
+                         "(per_config records); default: the whole range")
+    ap.add_argument("--no-configs", dest="configs", action="store_const", const="",
+                    help="measure only the headline workload (no per_config records)")
     ap.add_argument("--cpu-rows", type=int, default=128)
     ap.add_argument("--ref-rows", type=int, default=4)
     args = ap.parse_args()

@@ -69,7 +69,8 @@ class MSAStep:
 
 
 class HostInputStep:
-    """Training steps whose inputs arrive in pinned host memory.
+    """Training steps whose inputs arrive in, and whose results return to,
+    pinned host memory.
 
     The host-to-device copies run on a copy stream in the order the calls need
     them (cu_seqlens, q_p, k_p for the selection; k, v, q for the forward; dO
@@ -77,13 +78,22 @@ class HostInputStep:
     copies of the later inputs overlap the earlier kernels.  Two sets of device
     input buffers alternate between steps: the copies of step i also overlap
     the kernels of step i-1, and wait only for step i-2's kernels, the last to
-    read the set they overwrite.  Each step's proxy-KL loss is copied back to
-    pinned host memory on the compute stream; read it after synchronising.
-    The host tensors are read asynchronously: leave them unchanged until the
-    step's kernels have finished (for instance, until its loss has been read).
+    read the set they overwrite.
+
+    Results go back on a second copy stream: O (and LSE) as soon as the
+    forward has finished, so their copy overlaps the backward; the five
+    gradients and the proxy-KL loss after the backward, overlapping the next
+    step's selection and forward.  The next step's forward and backward wait
+    for those copies before overwriting the device outputs.  Without
+    `host_out`, only the loss is copied back (to `self.loss`).  Read host
+    results after synchronising.  The host tensors are read and written
+    asynchronously: leave the inputs unchanged, and do not read the outputs,
+    until the step's copies have finished.
     """
 
     GROUPS = (("cu_seqlens", "q_p", "k_p"), ("k", "v", "q"), ("dO",))
+    FWD_OUT = ("o", "lse")
+    BWD_OUT = ("dq", "dk", "dv", "dq_p", "dk_p", "kl_loss")
 
     def __init__(self, params, like: dict, device="cuda", step: MSAStep | None = None):
         """like: tensors with the shapes and dtypes of one step's inputs; step:
@@ -94,10 +104,20 @@ class HostInputStep:
                       for n in names} for _ in range(2)]
         self.done = [None, None]  # kernels of the last step that read buffer set b
         self.copy_stream = torch.cuda.Stream(device)
+        self.out_stream = torch.cuda.Stream(device)
         self.loss = torch.empty(1, dtype=torch.float64).pin_memory()
+        self._fwd_out_copied = None  # copies of the previous step's O / gradients
+        self._bwd_out_copied = None
         self._n = 0
 
-    def __call__(self, host_inp: dict, loss_out: torch.Tensor | None = None) -> dict:
+    def allocate_host_outputs(self) -> dict:
+        """Pinned host tensors for every result the step returns."""
+        out = self.step.out
+        return {n: torch.empty(out[n].shape, dtype=out[n].dtype).pin_memory()
+                for n in self.FWD_OUT + self.BWD_OUT}
+
+    def __call__(self, host_inp: dict, loss_out: torch.Tensor | None = None,
+                 host_out: dict | None = None) -> dict:
         """Queue one step on the current stream; returns the device outputs
         (valid until the next step's kernels overwrite them)."""
         for grp in self.GROUPS:
@@ -106,9 +126,14 @@ class HostInputStep:
                 if t.is_cuda or not t.is_pinned():
                     raise ValueError(f"HostInputStep: input {n!r} must be a pinned host tensor "
                                      "(pageable memory would make every copy synchronous)")
+        if host_out is not None:
+            for n in self.FWD_OUT + self.BWD_OUT:
+                t = host_out[n]
+                if t.is_cuda or not t.is_pinned():
+                    raise ValueError(f"HostInputStep: output {n!r} must be a pinned host tensor")
         b = self._n & 1
         self._n += 1
-        dev, cs = self.bufs[b], self.copy_stream
+        dev, cs, os_ = self.bufs[b], self.copy_stream, self.out_stream
         st = torch.cuda.current_stream(cs.device)
         if self.done[b] is not None:
             cs.wait_event(self.done[b])
@@ -120,18 +145,47 @@ class HostInputStep:
                 ev = torch.cuda.Event()
                 ev.record(cs)
                 ready.append(ev)
+        out = self.step.out
         st.wait_event(ready[0])
         self.step.select(dev, st)
         st.wait_event(ready[1])
+        if self._fwd_out_copied is not None:  # the previous step's O has left
+            st.wait_event(self._fwd_out_copied)
         self.step.forward(dev, st)
+        if host_out is not None:
+            fwd_done = torch.cuda.Event()
+            fwd_done.record(st)
+            os_.wait_event(fwd_done)
+            with torch.cuda.stream(os_):
+                for n in self.FWD_OUT:
+                    host_out[n].copy_(out[n], non_blocking=True)
+            self._fwd_out_copied = torch.cuda.Event()
+            self._fwd_out_copied.record(os_)
         st.wait_event(ready[2])
+        if self._bwd_out_copied is not None:  # the previous step's gradients have left
+            st.wait_event(self._bwd_out_copied)
         self.step.backward(dev, st)
-        (self.loss if loss_out is None else loss_out).copy_(self.step.out["kl_loss"],
-                                                            non_blocking=True)
         done = torch.cuda.Event()
         done.record(st)
         self.done[b] = done
-        return self.step.out
+        if host_out is None:
+            (self.loss if loss_out is None else loss_out).copy_(out["kl_loss"], non_blocking=True)
+        else:
+            os_.wait_event(done)
+            with torch.cuda.stream(os_):
+                for n in self.BWD_OUT:
+                    host_out[n].copy_(out[n], non_blocking=True)
+            self._bwd_out_copied = torch.cuda.Event()
+            self._bwd_out_copied.record(os_)
+        return out
+
+    def wait_outputs(self, stream=None) -> None:
+        """Makes `stream` (default: the current one) wait for the result copies
+        queued so far."""
+        st = stream if stream is not None else torch.cuda.current_stream(self.out_stream.device)
+        for ev in (self._fwd_out_copied, self._bwd_out_copied):
+            if ev is not None:
+                st.wait_event(ev)
 
 
 def run_step(params, inp, device="cuda") -> dict:

@@ -53,3 +53,35 @@ def test_host_input_step_rejects_pageable_inputs():
     hs = HostInputStep(params_for(inp["cu_seqlens"].tolist(), hq, hkv, d, dp, k), inp)
     with pytest.raises(ValueError):
         hs(inp)  # pageable CPU tensors
+
+
+def test_host_outputs_of_every_step_match_device_steps():
+    """With host_out, O, LSE, the five gradients and the loss of every step
+    come back to pinned host memory while later steps run; each step's copy
+    must hold that step's results bit for bit (a copy that a later step's
+    kernels overtook would hold the later step's values)."""
+    from block_sparse_attention_proxy_gb300 import msa_get_device_status
+    from block_sparse_attention_proxy_gb300.step import HostInputStep, MSAStep, params_for
+
+    lens, hq, hkv, d, dp, k = SHAPE
+    sets = [synth.make_inputs(synth.custom(lens, hq, hkv, d, dp, k, seed=70 + i, structured=True))
+            for i in range(3)]
+    prm = params_for(sets[0]["cu_seqlens"].tolist(), hq, hkv, d, dp, k)
+    ref = []
+    st = MSAStep(prm)
+    for inp in sets:
+        out = st({n: v.cuda() for n, v in inp.items()})
+        torch.cuda.synchronize()
+        ref.append({n: v.cpu() for n, v in out.items()})
+    host = [{n: v.pin_memory() for n, v in inp.items()} for inp in sets]
+    hs = HostInputStep(prm, sets[0])
+    order = [0, 1, 2, 0, 1]
+    outs = [hs.allocate_host_outputs() for _ in order]
+    for j, i in enumerate(order):
+        hs(host[i], host_out=outs[j])
+    hs.wait_outputs()
+    torch.cuda.synchronize()
+    assert msa_get_device_status() == 0
+    for j, i in enumerate(order):
+        for n in HostInputStep.FWD_OUT + HostInputStep.BWD_OUT:
+            assert torch.equal(outs[j][n], ref[i][n]), (j, i, n)
