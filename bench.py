@@ -91,12 +91,14 @@ def kernel_models(w, c) -> dict:
     """Algorithmic work per launch of the three block kernels.
 
     select (tensor-bound): 2*dp FLOPs per causal (query, key) pair per group.
-    fwd (HBM-bound): per (token, head, slot): gathered q row (2d B), fp32 partial
-        O write (4d B) and lse (4 B); per (group, block): K and V tiles (2*128*2d B).
+    fwd (HBM-bound): per (token, head, slot): gathered q row (2d B), partial O
+        row written as int16 (2d B) with its lse and scale (8 B); per (group,
+        block): K and V tiles (2*128*2d B).
     bwd (HBM-bound): per (token, head, slot): q and dO rows (4d B), fp32 dQ
         partial (4d B), lse and D (8 B); per (token, group, slot): q_p row and
-        proxy scalars (2dp + 13 B); per (group, block): K, V reads (4*128*d B),
-        dK, dV writes (8*128*d B), dk_p write (4*128*dp B).
+        proxy scalars (2dp + 13 B);
+        per (group, block): K, V reads (4*128*d B), dK, dV writes (8*128*d B),
+        dk_p write (4*128*dp B).
     """
     d, dp, hq, hkv = w.d, w.dp, w.hq, w.hkv
     rs = c["rowslots"] * hq
@@ -105,7 +107,7 @@ def kernel_models(w, c) -> dict:
     return {
         1: dict(name="k_select", bound="tensor", work=2.0 * dp * hkv * c["causal"], unit="TFLOP/s"),
         2: dict(name="k_fwd", bound="hbm",
-                work=rs * (6.0 * d + 4) + blk * (4.0 * 128 * d), unit="GB/s"),
+                work=rs * (4.0 * d + 8) + blk * (4.0 * 128 * d), unit="GB/s"),
         3: dict(name="k_bwd", bound="hbm",
                 work=rs * (8.0 * d + 8) + ts * (2.0 * dp + 13) +
                 blk * (4.0 * 128 * d + 8.0 * 128 * d + 4.0 * 128 * dp), unit="GB/s"),

@@ -17,11 +17,11 @@ import ctypes
 
 import torch
 
-from ._abi import (EXPORTS, LIB_PATH, MSA_FLAG_REUSE_REGROUP, MSA_OK, MsaError, MsaParams,
-                   STATUS_NAMES, load)
+from ._abi import (EXPORTS, LIB_PATH, MSA_FLAG_REUSE_REGROUP, MSA_FLAG_TEST_STALL_SELECT, MSA_OK,
+                   MsaError, MsaParams, STATUS_NAMES, load)
 
 __all__ = [
-    "MsaError", "MsaParams", "MSA_FLAG_REUSE_REGROUP", "make_params", "msa_select_workspace_size", "msa_fwd_workspace_size",
+    "MsaError", "MsaParams", "MSA_FLAG_REUSE_REGROUP", "MSA_FLAG_TEST_STALL_SELECT", "make_params", "msa_select_workspace_size", "msa_fwd_workspace_size",
     "msa_bwd_workspace_size", "msa_proxy_select", "msa_proxy_select_noalloc", "msa_fwd", "msa_bwd", "msa_get_device_status",
     "msa_last_status_word", "msa_launch_count", "msa_set_profile_events", "msa_status_string", "allocate_outputs", "workspace", "EXPORTS", "LIB_PATH", "load",
 ]

@@ -9,6 +9,7 @@ LIB_PATH = os.path.join(_PKG, "libmsa.so")
 
 MSA_OK = 0
 MSA_FLAG_REUSE_REGROUP = 0x1  # msa_bwd: reuse the block lists msa_fwd left in the workspace
+MSA_FLAG_TEST_STALL_SELECT = 0x100  # test hook: the selection kernel's first wait runs out
 STATUS_NAMES = {
     0: "MSA_OK",
     1: "MSA_ERR_INVALID_ARG",

@@ -526,12 +526,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint8_t* dsl = dsh + 16384;
       dead = dead || !wait_bar_warp(bar(B_MF + s), (n / NM) & 1, abort_flag, a.status,
                                     wait_site(kKerBwd, B_MF + s, n));
+      if (!dead) {
+        // fused proxy gradient (needs only the tile's records and q_p rows, so
+        // it runs while the S^T/dP^T products are in flight): every token of the
+        // tile adds g_b q_p[t] to the dk_p row of its block argmax; the warp
+        // owning that key takes it, one dimension per lane (tokens in list
+        // order, so the sum is deterministic)
+        for (int base = 0; base < cnt; base += 32) {
+          const int i = base + lane;
+          int ai = -1;
+          float gi = 0.f;
+          if (i < cnt) {
+            const int4 hd = *reinterpret_cast<const int4*>(rec + i * kRec);
+            if (hd.x < a.T) {
+              ai = hd.z;
+              gi = __int_as_float(hd.w);
+            }
+          }
+          uint32_t mine = __ballot_sync(0xffffffffu, ai >= 0 && (ai >> 5) == (warp & 3));
+          while (mine) {
+            const int j = __ffs(mine) - 1;
+            mine &= mine - 1;
+            const int aj = __shfl_sync(0xffffffffu, ai, j);
+            const float gj = __shfl_sync(0xffffffffu, gi, j);
+            const float qv =
+                lane < DPH ? __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
+                                                 stP(s) + (base + j) * C::kQpRow +
+                                                 (DPH * e + lane) * 2)
+                                             << 16)
+                           : 0.f;
+            add_at32(kacc, aj & 31, gj * qv);
+          }
+        }
+      }
       dead = dead || !wait_bar_warp(bar(B_SP + b), (n >> 1) & 1, abort_flag, a.status,
                                     wait_site(kKerBwd, B_SP + b, n));
       tc_fence_after();
       if (!dead) {
         const uint32_t ts = tbase + lane_off + 128u * b;
-        uint32_t pw[16];  // P^T of this warpgroup's 32 rows, bf16 pairs
+        // P^T and dS^T of this warpgroup's 32 rows (bf16 pairs); the dS^T
+        // stores are the only step that waits for the previous tile's products
+        uint32_t pw[16], dh[16], dl[16];
         // this warpgroup's rows start at token 32e/G of the tile; every offset
         // below is a compile-time constant
         const uint8_t* recw = rec + (32 * e / G) * kRec + 16;
@@ -541,7 +576,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int r0 = 32 * e + 16 * q16;
           uint32_t sv[16], dv[16];
           tmem_ld16x2(ts + r0, ts + 64 + r0, sv, dv);
-          uint32_t dh[8], dl[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float pv[2];
@@ -575,53 +609,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               lb[u] = __float_as_uint(ds - __uint_as_float(hb[u] & 0xFFFF0000u));
             }
             pw[8 * q16 + i] = pack_bf16(pv[0], pv[1]);
-            dh[i] = pack_hi_halves(hb[0], hb[1]);
-            dl[i] = pack_hi_halves(lb[0], lb[1]);
-          }
-          // the dS^T buffer was last read by the products of tile n-1, which
-          // normally completed while the first half was computed
-          if (q16 == 0 && n >= 1)
-            dead = !wait_bar_warp(bar(B_DQ + ((n - 1) & 1)), ((n - 1) >> 1) & 1, abort_flag,
-                                  a.status, wait_site(kKerBwd, B_DQ + ((n - 1) & 1), n));
-          if (dead) continue;
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const uint32_t off = sw128_offset((uint32_t)kk, (uint32_t)(r0 / 8 + q));
-            *reinterpret_cast<uint4*>(dsh + off) =
-                make_uint4(dh[4 * q], dh[4 * q + 1], dh[4 * q + 2], dh[4 * q + 3]);
-            *reinterpret_cast<uint4*>(dsl + off) =
-                make_uint4(dl[4 * q], dl[4 * q + 1], dl[4 * q + 2], dl[4 * q + 3]);
+            dh[8 * q16 + i] = pack_hi_halves(hb[0], hb[1]);
+            dl[8 * q16 + i] = pack_hi_halves(lb[0], lb[1]);
           }
         }
         // P^T into this warpgroup's half of the dP^T columns (already read)
-        if (!dead) tmem_st16(ts + 64 + 32 * e, pw);
-        // fused proxy gradient: every token of the tile adds g_b q_p[t] to the
-        // dk_p row of its block argmax; the warp owning that key takes it, one
-        // dimension per lane (tokens in list order, so the sum is deterministic)
-        for (int base = 0; base < (dead ? 0 : cnt); base += 32) {
-          const int i = base + lane;
-          int ai = -1;
-          float gi = 0.f;
-          if (i < cnt) {
-            const int4 hd = *reinterpret_cast<const int4*>(rec + i * kRec);
-            if (hd.x < a.T) {
-              ai = hd.z;
-              gi = __int_as_float(hd.w);
+        tmem_st16(ts + 64 + 32 * e, pw);
+        // the dS^T buffer was last read by the products of tile n-1
+        if (n >= 1)
+          dead = !wait_bar_warp(bar(B_DQ + ((n - 1) & 1)), ((n - 1) >> 1) & 1, abort_flag,
+                                a.status, wait_site(kKerBwd, B_DQ + ((n - 1) & 1), n));
+        if (!dead) {
+#pragma unroll
+          for (int q16 = 0; q16 < 2; ++q16) {
+            const int r0 = 32 * e + 16 * q16;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const uint32_t off = sw128_offset((uint32_t)kk, (uint32_t)(r0 / 8 + q));
+              const int w0 = 8 * q16 + 4 * q;
+              *reinterpret_cast<uint4*>(dsh + off) =
+                  make_uint4(dh[w0], dh[w0 + 1], dh[w0 + 2], dh[w0 + 3]);
+              *reinterpret_cast<uint4*>(dsl + off) =
+                  make_uint4(dl[w0], dl[w0 + 1], dl[w0 + 2], dl[w0 + 3]);
             }
-          }
-          uint32_t mine = __ballot_sync(0xffffffffu, ai >= 0 && (ai >> 5) == (warp & 3));
-          while (mine) {
-            const int j = __ffs(mine) - 1;
-            mine &= mine - 1;
-            const int aj = __shfl_sync(0xffffffffu, ai, j);
-            const float gj = __shfl_sync(0xffffffffu, gi, j);
-            const float qv =
-                lane < DPH ? __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
-                                                 stP(s) + (base + j) * C::kQpRow +
-                                                 (DPH * e + lane) * 2)
-                                             << 16)
-                           : 0.f;
-            add_at32(kacc, aj & 31, gj * qv);
           }
         }
       }

@@ -13,8 +13,9 @@
 // columns in place of each 32 score columns, so no unread score is
 // overwritten), and O = P_hi V + P_lo V reads P straight from TMEM; O keeps
 // ~16 mantissa bits of P, which the backward's D = rowsum(dO * O) needs.  The
-// normalised partial O_slot and lse_slot (both fp32) are written per (token,
-// head, slot); the merge kernel combines the slots by log-sum-exp.
+// normalised partial O_slot is written per (token, head, slot) as 16-bit fixed
+// point relative to the row's max |O_slot| (int16 row + fp32 scale, beside
+// lse_slot); the merge kernel combines the slots by log-sum-exp.
 //
 // Roles (320 threads): two softmax warpgroups (warps 0-3 and 4-7) take
 // alternate tiles through two S/O accumulator pairs, so one warpgroup's
@@ -30,9 +31,9 @@ namespace {
 
 constexpr int kFwdThreads = 320;
 constexpr int kFwdQStages = 3;
-// Per softmax warp: a 32-row x 32-column fp32 staging tile (128B-swizzled
+// Per softmax warp: a 32-row x 64-column int16 staging tile (128B-swizzled
 // rows) and the 32 row pointers, used to turn row-per-thread O values into
-// row-contiguous 512-byte warp stores.
+// row-contiguous 128-byte segments, four rows per warp store.
 constexpr int kFwdStageWarp = 4096 + 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -43,8 +44,8 @@ struct FwdArgs {
   const uint32_t* ent;
   int ndoc, T, hq, hkv, K, nb_bound;
   float scale;
-  float* o_part;    // rows of the query chunk: token - t0
-  float* lse_part;
+  int16_t* o_part;  // [tokens of the query chunk (token - t0)][hq][K][D] int16
+  float2* o_meta;   // [..][hq][K] {lse_slot, dequantisation scale}
   unsigned* status;
   int chunk;        // query chunk (qchunk_of)
   int qcb;          // KV blocks per query chunk
@@ -331,37 +332,53 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                     wait_site(kKerFwd, b_ofull(b), n));
       tc_fence_after();
       if (!dead) {
-        // O row (this thread's) in 32-column chunks: TMEM -> registers (scaled
-        // by 1/l) -> swizzled staging tile -> each warp store writes 4 rows x
-        // 128 contiguous bytes.
-        const float inv_l = 1.f / l;
+        // O row (this thread's): a first pass over TMEM finds max |O|, a second
+        // writes it as 16-bit fixed point, 64 columns per TMEM round trip:
+        // registers -> swizzled staging tile -> each warp store writes 4 rows
+        // x 128 contiguous bytes.
         const uint32_t to = tbase + lane_off + 256 + b * D;
-        uint8_t* stg = sOst + warp * kFwdStageWarp;
-        float** rowp = reinterpret_cast<float**>(stg + 4096);
-        rowp[lane] = valid ? a.o_part + (((size_t)(t - t0) * a.hq + g * G + hl) * a.K + slot) * (size_t)D
-                           : nullptr;
+        uint32_t mbits = 0;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float v[32];
-          tmem_ld32f(to + c * 32, v);
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t va[32], vb[32];
+          tmem_ld32x2(to + c * 64, to + c * 64 + 32, va, vb);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mbits = max(mbits, max(abs_bits(va[i]), abs_bits(vb[i])));
+        }
+        const float mo = __uint_as_float(mbits);
+        const float qf = q16_factor(mo);
+        uint8_t* stg = sOst + warp * kFwdStageWarp;
+        int16_t** rowp = reinterpret_cast<int16_t**>(stg + 4096);
+        const size_t prow = ((size_t)(t - t0) * a.hq + g * G + hl) * a.K + slot;
+        rowp[lane] = valid ? a.o_part + prow * (size_t)D : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t va[32], vb[32];
+          tmem_ld32x2(to + c * 64, to + c * 64 + 32, va, vb);
+          uint32_t w[32];  // columns 64c .. 64c+63 as int16 pairs
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_q16x2(__uint_as_float(va[2 * i]) * qf, __uint_as_float(va[2 * i + 1]) * qf);
+            w[16 + i] =
+                pack_q16x2(__uint_as_float(vb[2 * i]) * qf, __uint_as_float(vb[2 * i + 1]) * qf);
+          }
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) =
-                make_float4(v[4 * q] * inv_l, v[4 * q + 1] * inv_l, v[4 * q + 2] * inv_l,
-                            v[4 * q + 3] * inv_l);
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           __syncwarp();
           const int ch = lane & 7;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int rr = (lane >> 3) + 4 * i;
-            const float4 x = *reinterpret_cast<const float4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
-            float* dst = rowp[rr];
-            if (dst != nullptr) *reinterpret_cast<float4*>(dst + c * 32 + ch * 4) = x;
+            const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
+            int16_t* dst = rowp[rr];
+            if (dst != nullptr) *reinterpret_cast<uint4*>(dst + c * 64 + ch * 8) = x;
           }
           __syncwarp();
         }
-        if (valid)
-          a.lse_part[((size_t)(t - t0) * a.hq + g * G + hl) * a.K + slot] = mx * a.scale + __logf(l);
+        // O_slot = O / l, so the row's factor is max|O| / (32767 l)
+        if (valid) a.o_meta[prow] = make_float2(mx * a.scale + __logf(l), mo / (kQ16 * l));
       }
       tc_fence_before();
       __syncwarp();
@@ -408,7 +425,7 @@ cudaError_t launch_fwd_d(const Shape& s, const CUtensorMap& mq, const CUtensorMa
 
 cudaError_t launch_fwd(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
                        const int32_t* row_ptr, const uint32_t* ent, const uint16_t* q,
-                       const uint16_t* k, const uint16_t* v, float* o_part, float* lse_part,
+                       const uint16_t* k, const uint16_t* v, int16_t* o_part, float2* o_meta,
                        int chunk, unsigned* status, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   cudaError_t e;
@@ -416,7 +433,7 @@ cudaError_t launch_fwd(const Shape& s, const int32_t* cu_seqlens, const int32_t*
   if ((e = make_tmap_3d(&mk, k, s.d, s.hkv, s.T, 64, 1, 128, 128)) != cudaSuccess) return e;
   if ((e = make_tmap_3d(&mv, v, s.d, s.hkv, s.T, 64, 1, 128, 128)) != cudaSuccess) return e;
   FwdArgs a{cu_seqlens, cu_blocks, row_ptr, ent,   s.ndoc, s.T,   s.hq,
-            s.hkv,      s.K,       s.nb_bound, s.softmax_scale, o_part, lse_part, status,
+            s.hkv,      s.K,       s.nb_bound, s.softmax_scale, o_part, o_meta,   status,
             chunk,      s.qc_blocks};
   return s.d == 128 ? launch_fwd_d<128>(s, mq, mk, mv, a, st)
                     : launch_fwd_d<64>(s, mq, mk, mv, a, st);

@@ -1,7 +1,8 @@
 // Memory-bound epilogues of the forward and backward passes.
 //
 //   k_fwd_merge   per (token, group): log-sum-exp merge of the per-slot partials
-//                 of every head (O, LSE), and the target mass of the proxy loss
+//                 of every head (O as 16-bit fixed point with a per-row scale,
+//                 lse), and the target mass of the proxy loss
 //                 m_b = (1/G) sum_h exp(lse_{h,b} - LSE_h) per selected block.
 //                 It also writes o_res = bf16(O - bf16(O)), the rounding residual
 //                 of the bf16 output, so the backward can form D from ~16 bits of O.
@@ -28,9 +29,9 @@ template <int D>
 __global__ void __launch_bounds__(kRedWarps * 32)
     k_fwd_merge(int T, int ndoc, const int32_t* __restrict__ cu,
                 const int32_t* __restrict__ cu_blocks, int nb_bound, int chunk, int qcb, int hkv,
-                int G, int K, const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                uint16_t* __restrict__ o, uint16_t* __restrict__ o_res, float* __restrict__ lse,
-                float* __restrict__ mass) {
+                int G, int K, const int16_t* __restrict__ o_part,
+                const float2* __restrict__ o_meta, uint16_t* __restrict__ o,
+                uint16_t* __restrict__ o_res, float* __restrict__ lse, float* __restrict__ mass) {
   constexpr int PER = D / 32;  // head-dim elements per lane
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kRedWarps + (threadIdx.x >> 5);
@@ -50,40 +51,42 @@ __global__ void __launch_bounds__(kRedWarps * 32)
   for (int hh = 0; hh < G; ++hh) {
     const size_t row = (size_t)t * hq + g * G + hh;
     const size_t prow = (size_t)(t - t0) * hq + g * G + hh;
-    const float ls = lane < nsel ? __ldg(lse_part + prow * K + lane) : -INFINITY;
+    const float2 meta = lane < nsel ? __ldg(o_meta + prow * K + lane)
+                                    : make_float2(-INFINITY, 0.f);
     // every slot's partial is requested before any is used
-    const float* src = o_part + prow * K * (size_t)D + lane * PER;
-    float x[kMaxTopK][PER];
+    const int16_t* src = o_part + prow * K * (size_t)D + lane * PER;
+    uint32_t x[kMaxTopK][PER / 2];
 #pragma unroll
     for (int s = 0; s < kMaxTopK; ++s) {
       if (s < nsel) {
         if (PER == 4) {
-          const float4 v4 = __ldg(reinterpret_cast<const float4*>(src + (size_t)s * D));
-          x[s][0] = v4.x;
-          x[s][1] = v4.y;
-          x[s][PER > 2 ? 2 : 0] = v4.z;
-          x[s][PER > 3 ? 3 : 0] = v4.w;
-        } else {
-          const float2 v2 = __ldg(reinterpret_cast<const float2*>(src + (size_t)s * D));
+          const uint2 v2 = __ldg(reinterpret_cast<const uint2*>(src + (size_t)s * D));
           x[s][0] = v2.x;
-          x[s][1] = v2.y;
+          x[s][PER / 2 - 1] = v2.y;
+        } else {
+          x[s][0] = __ldg(reinterpret_cast<const unsigned int*>(src + (size_t)s * D));
         }
       }
     }
+    const float ls = meta.x;
     const float mx = warp_max(ls);
     const float se = warp_sum(lane < nsel ? __expf(ls - mx) : 0.f);
     const float LSE = mx + __logf(se);
     const float w = lane < nsel ? __expf(ls - LSE) : 0.f;
     macc += w;
+    const float wq = w * meta.y;  // merge weight times the slot row's scale
     float acc[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u) acc[u] = 0.f;
 #pragma unroll
     for (int s = 0; s < kMaxTopK; ++s) {
-      const float ws = __shfl_sync(0xffffffffu, w, s);
+      const float ws = __shfl_sync(0xffffffffu, wq, s);
       if (s < nsel) {
 #pragma unroll
-        for (int u = 0; u < PER; ++u) acc[u] = fmaf(ws, x[s][u], acc[u]);
+        for (int u = 0; u < PER / 2; ++u) {
+          acc[2 * u] = fmaf(ws, q16_lo(x[s][u]), acc[2 * u]);
+          acc[2 * u + 1] = fmaf(ws, q16_hi(x[s][u]), acc[2 * u + 1]);
+        }
       }
     }
     uint16_t* dst = o + row * D + lane * PER;
@@ -273,7 +276,7 @@ __global__ void __launch_bounds__(1024) k_kl_final(int n, const double* __restri
 }  // namespace
 
 cudaError_t launch_fwd_merge(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
-                             const float* o_part, const float* lse_part, uint16_t* o,
+                             const int16_t* o_part, const float2* o_meta, uint16_t* o,
                              uint16_t* o_res, float* lse, float* mass, int chunk,
                              cudaStream_t st) {
   const long long warps = (long long)s.T * s.hkv;
@@ -281,12 +284,12 @@ cudaError_t launch_fwd_merge(const Shape& s, const int32_t* cu_seqlens, const in
   if (s.d == 128)
     k_fwd_merge<128><<<blocks, kRedWarps * 32, 0, st>>>(s.T, s.ndoc, cu_seqlens, cu_blocks,
                                                          s.nb_bound, chunk, s.qc_blocks, s.hkv,
-                                                         s.G, s.K, o_part, lse_part, o, o_res,
+                                                         s.G, s.K, o_part, o_meta, o, o_res,
                                                          lse, mass);
   else
     k_fwd_merge<64><<<blocks, kRedWarps * 32, 0, st>>>(s.T, s.ndoc, cu_seqlens, cu_blocks,
                                                         s.nb_bound, chunk, s.qc_blocks, s.hkv,
-                                                        s.G, s.K, o_part, lse_part, o, o_res,
+                                                        s.G, s.K, o_part, o_meta, o, o_res,
                                                         lse, mass);
   return cudaGetLastError();
 }

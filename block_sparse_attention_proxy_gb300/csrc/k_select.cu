@@ -13,12 +13,16 @@
 // list, its lowest-index argmax.  Neither the score tile nor the pooled
 // [T, blocks] matrix ever leaves the SM.
 //
-// Roles (320 threads): warps 0-3 and 4-7 are two epilogue warpgroups, warp 8
-// issues TMA loads of k_p into a ring, warp 9 issues tcgen05.mma.  Key blocks
-// go in steps of two: one 256-row k_p box per step, one N = 256 MMA chain
-// into a 256-column TMEM accumulator, and each warpgroup takes every other
-// step with its own accumulator.  The fixed cost of a step (barrier hand-offs,
-// commits) is paid once per two blocks.
+// Roles (512 threads): warps 0-11 are three epilogue warpgroups, warp 12
+// issues TMA loads of k_p into a ring, warp 13 issues tcgen05.mma, warps 14-15
+// idle.  Key blocks go in steps of two: one 256-row k_p box per step, one
+// N = 256 MMA chain into one of two 256-column TMEM accumulators (steps
+// alternate), so the fixed cost of a step (barrier hand-offs, commits) is paid
+// once per two blocks.  Block n goes to epilogue warpgroup n mod 3: three
+// warpgroups keep the max trees of the blocks fed to the tensor core (with two,
+// the tensor pipe waited on the epilogue more than half of the time), and a
+// step's accumulator is released once both of its blocks have been read.
+// Register budgets per warpgroup: 3 x 128 x 152 (epilogue) + 128 x 56 = 65536.
 //
 // Block pattern: with a window (w, s) the blocks J - s*u, u = 1..w, are kept
 // whatever their score; the pattern is configurable by window size and
@@ -35,7 +39,10 @@ namespace msa {
 namespace {
 
 constexpr int kSelStages = 4;  // k_p ring stages, two key blocks each
-constexpr int kSelThreads = 320;
+constexpr int kSelThreads = 512;
+constexpr int kSelEpiGroups = 3;
+constexpr int kSelProducerWarp = 12, kSelMmaWarp = 13;
+constexpr uint32_t kSelRegsEpi = 152, kSelRegsCtl = 56;
 constexpr float kTieBand = 1e-3f;
 
 template <int DP>
@@ -120,6 +127,7 @@ struct SelArgs {
   float* plse;
   uint8_t* tie;
   unsigned* status;
+  bool withhold_q;  // test hook: never load the query tile (the MMA warp's wait runs out)
 };
 
 template <int DP, int CAP, bool ARG, bool WIN>
@@ -133,9 +141,10 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   // ---- shared memory carve-up ----
   uint8_t* sQ = smem;                                   // q_p tile, 128 rows
   uint8_t* sK = sQ + C::kTileBytes;                     // k_p ring: pairs of 128-key blocks
-  float* m_sc = reinterpret_cast<float*>(sK + kSelStages * 2 * C::kTileBytes);  // [CAP][128]
-  uint32_t* m_id = reinterpret_cast<uint32_t*>(m_sc + CAP * 128);           // [CAP][128]
-  float* d_sc = reinterpret_cast<float*>(m_id + CAP * 128);                 // [128]
+  // lists of warpgroups 1 and 2 for the merge: [2][CAP][128]
+  float* m_sc = reinterpret_cast<float*>(sK + kSelStages * 2 * C::kTileBytes);
+  uint32_t* m_id = reinterpret_cast<uint32_t*>(m_sc + 2 * CAP * 128);
+  float* d_sc = reinterpret_cast<float*>(m_id + 2 * CAP * 128);             // [128]
   uint32_t* d_id = reinterpret_cast<uint32_t*>(d_sc + 128);                 // [128]
   // [CAP][128] always-kept blocks (block pattern only)
   float* f_sc = reinterpret_cast<float*>(d_id + 128);
@@ -175,12 +184,12 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_accfull(i), 1);
-      mbar_init(b_accempty(i), 4);
+      mbar_init(b_accempty(i), 8);  // four warps for each of the step's two blocks
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == kSelMmaWarp) {
     tmem_alloc(smem_u32(tslot), 512);
     tmem_relinquish();
   }
@@ -189,57 +198,70 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(tslot);
 
-  if (warp == 8) {
-    // ------------------------------ TMA producer ------------------------------
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_qp);
-      tma_prefetch_desc(&tm_kp);
-      mbar_arrive_expect_tx(b_qfull, C::kTileBytes);
-      tma_load_3d(smem_u32(sQ), &tm_qp, b_qfull, 0, g, qstart);
-      // step m: key blocks 2m and 2m+1 as one 256-row box (rows past the
-      // diagonal block, or past T, are loaded or zero-filled and never read)
-      for (int m = 0; m < nstep; ++m) {
-        const int s = m % kSelStages;
-        if (m >= kSelStages &&
-            !wait_bar(b_kvempty(s), ((m / kSelStages) & 1) ^ 1, abort_flag, a.status,
-                      wait_site(kKerSelect, 7 + s, m)))
-          break;
-        mbar_arrive_expect_tx(b_kvfull(s), 2 * C::kTileBytes);
-        tma_load_3d(smem_u32(sK + s * 2 * C::kTileBytes), &tm_kp, b_kvfull(s), 0, g,
-                    dstart + 2 * m * kBlock);
-      }
-    }
-  } else if (warp == 9) {
-    // ------------------------------ MMA issuer ---------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(128, 256, false, false);
-      if (wait_bar(b_qfull, 0, abort_flag, a.status, wait_site(kKerSelect, 0, 0))) {
-        const uint32_t q0 = smem_u32(sQ);
+  if (warp >= 4 * kSelEpiGroups) {
+    setmaxnreg_dec<kSelRegsCtl>();
+    if (warp == kSelProducerWarp) {
+      // ------------------------------ TMA producer ------------------------------
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_qp);
+        tma_prefetch_desc(&tm_kp);
+        if (!a.withhold_q) {
+          mbar_arrive_expect_tx(b_qfull, C::kTileBytes);
+          tma_load_3d(smem_u32(sQ), &tm_qp, b_qfull, 0, g, qstart);
+        }
+        // step m: key blocks 2m and 2m+1 as one 256-row box (rows past the
+        // diagonal block, or past T, are loaded or zero-filled and never read)
+        int issued = 0;
         for (int m = 0; m < nstep; ++m) {
-          const int s = m % kSelStages, acc = m & 1;
-          if (!wait_bar(b_kvfull(s), (m / kSelStages) & 1, abort_flag, a.status,
-                        wait_site(kKerSelect, 1 + s, m)))
+          const int s = m % kSelStages;
+          if (m >= kSelStages &&
+              !wait_bar(b_kvempty(s), ((m / kSelStages) & 1) ^ 1, abort_flag, a.status,
+                        wait_site(kKerSelect, 7 + s, m)))
             break;
-          if (m >= 2 && !wait_bar(b_accempty(acc), ((m >> 1) & 1) ^ 1, abort_flag, a.status,
-                                  wait_site(kKerSelect, 17 + acc, m)))
-            break;
-          tc_fence_after();
-          const uint32_t k0 = smem_u32(sK + s * 2 * C::kTileBytes);
-          // scores of 128 queries x 256 keys (two blocks) into a 256-column accumulator
+          mbar_arrive_expect_tx(b_kvfull(s), 2 * C::kTileBytes);
+          tma_load_3d(smem_u32(sK + s * 2 * C::kTileBytes), &tm_kp, b_kvfull(s), 0, g,
+                      dstart + 2 * m * kBlock);
+          issued = m + 1;
+        }
+        // Let this CTA's own copies land before it exits (they have, unless a
+        // wait gave up): the last use of every ring stage, and the query tile.
+        for (int m = issued > kSelStages ? issued - kSelStages : 0; m < issued; ++m)
+          drain_bar(b_kvfull(m % kSelStages), (m / kSelStages) & 1);
+        if (!a.withhold_q) drain_bar(b_qfull, 0);
+      }
+    } else if (warp == kSelMmaWarp) {
+      // ------------------------------ MMA issuer ---------------------------------
+      if (lane == 0) {
+        constexpr uint32_t idesc = make_idesc_bf16(128, 256, false, false);
+        if (wait_bar(b_qfull, 0, abort_flag, a.status, wait_site(kKerSelect, 0, 0))) {
+          const uint32_t q0 = smem_u32(sQ);
+          for (int m = 0; m < nstep; ++m) {
+            const int s = m % kSelStages, acc = m & 1;
+            if (!wait_bar(b_kvfull(s), (m / kSelStages) & 1, abort_flag, a.status,
+                          wait_site(kKerSelect, 1 + s, m)))
+              break;
+            if (m >= 2 && !wait_bar(b_accempty(acc), ((m >> 1) & 1) ^ 1, abort_flag, a.status,
+                                    wait_site(kKerSelect, 17 + acc, m)))
+              break;
+            tc_fence_after();
+            const uint32_t k0 = smem_u32(sK + s * 2 * C::kTileBytes);
+            // scores of 128 queries x 256 keys (two blocks) into a 256-column accumulator
 #pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint64_t ad = make_sdesc(q0 + kk * 32, 16, C::kSBO, C::kLayout);
-            const uint64_t bd = make_sdesc(k0 + kk * 32, 16, C::kSBO, C::kLayout);
-            umma_bf16(tbase + acc * 256, ad, bd, idesc, kk > 0);
+            for (int kk = 0; kk < DP / 16; ++kk) {
+              const uint64_t ad = make_sdesc(q0 + kk * 32, 16, C::kSBO, C::kLayout);
+              const uint64_t bd = make_sdesc(k0 + kk * 32, 16, C::kSBO, C::kLayout);
+              umma_bf16(tbase + acc * 256, ad, bd, idesc, kk > 0);
+            }
+            umma_commit(b_kvempty(s));
+            umma_commit(b_accfull(acc));
           }
-          umma_commit(b_kvempty(s));
-          umma_commit(b_accfull(acc));
         }
       }
     }
   } else {
+    setmaxnreg_inc<kSelRegsEpi>();
     // ------------------------------ epilogue -----------------------------------
-    const int e = warp >> 2;            // warpgroup 0 or 1
+    const int e = warp >> 2;            // warpgroup 0, 1 or 2
     const int row = (warp & 3) * 32 + lane;  // TMEM lane = query row in the block
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     float sc[CAP];
@@ -258,113 +280,107 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     // increasing order) pass it, so the block loop needs no division.
     int next_kept = INT_MAX;
     if (WIN && J >= a.dilation) next_kept = J - a.dilation * min(a.window, J / a.dilation);
-    // Warpgroup e takes the steps m = e, e + 2, ... (its own 256-column
-    // accumulator e); each step holds key blocks 2m and 2m + 1.
-    bool stop = false;
-    for (int m = e; !stop && m < nstep; m += 2) {
-      const int acc = m & 1;
-      if (!wait_bar_warp(b_accfull(acc), (m >> 1) & 1, abort_flag, a.status,
-                         wait_site(kKerSelect, 13 + acc, m))) {
-        stop = true;
-        break;
-      }
-      tc_fence_after();
+    // Warpgroup e takes the blocks n = e, e + 3, ... in increasing order; block
+    // n sits in half n & 1 of accumulator (n >> 1) & 1.
 #pragma unroll 1
-      for (int u = 0; u < 2; ++u) {
-        const int n = 2 * m + u;
-        if (n >= nblk) break;  // warp-uniform
-        const bool last = u == 1 || n + 1 >= nblk;
-        const uint32_t tb = tbase + lane_off + acc * 256 + u * 128;
-        const bool diag = (n == J);
-        // block of the always-kept window (warp-uniform)
-        bool forced = false;
-        if (WIN && !diag && n >= next_kept) {
-          while (next_kept < n) next_kept += a.dilation;
-          forced = n == next_kept;
-        }
-        // argmax bookkeeping for every block (ARG), else for the diagonal block only
-        const bool track = ARG || diag;  // warp-uniform
-        // The 32 scores of the chunk holding the row maximum stay in registers (first chunk
-        // on ties), so the argmax needs no second TMEM read.
-        uint32_t bv[32];
-        float best = 0.f;
-        int bc = 0;
+    for (int n = e; n < nblk; n += kSelEpiGroups) {
+      const int m = n >> 1, acc = m & 1, u = n & 1;
+      if (!wait_bar_warp(b_accfull(acc), (m >> 1) & 1, abort_flag, a.status,
+                         wait_site(kKerSelect, 13 + acc, m)))
+        break;
+      tc_fence_after();
+      const uint32_t tb = tbase + lane_off + acc * 256 + u * 128;
+      const bool diag = (n == J);
+      // block of the always-kept window (warp-uniform)
+      bool forced = false;
+      if (WIN && !diag && n >= next_kept) {
+        while (next_kept < n) next_kept += a.dilation;
+        forced = n == next_kept;
+      }
+      // argmax bookkeeping for every block (ARG), else for the diagonal block only
+      const bool track = ARG || diag;  // warp-uniform
+      // The 32 scores of the chunk holding the row maximum stay in registers (first chunk
+      // on ties), so the argmax needs no second TMEM read.
+      uint32_t bv[32];
+      float best = 0.f;
+      int bc = 0;
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {  // 64 columns per TMEM round trip
-          uint32_t va[32], vb[32];
-          tmem_ld32x2(tb + c2 * 64, tb + c2 * 64 + 32, va, vb);
-          if (diag) {
-            const uint32_t neg = __float_as_uint(-FLT_MAX);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (c2 * 64 + i > row) va[i] = neg;
-              if (c2 * 64 + 32 + i > row) vb[i] = neg;
-            }
-          }
-          const float ma = max32(va), mb = max32(vb);
-          if (c2 == 0) {
-            const bool tb1 = mb > ma;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (track) bv[i] = tb1 ? vb[i] : va[i];
-            best = tb1 ? mb : ma;
-            bc = tb1 ? 1 : 0;
-          } else {
-            const bool ta = ma > best;
-            const float m2 = ta ? ma : best;
-            const bool tb1 = mb > m2;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (track) bv[i] = tb1 ? vb[i] : (ta ? va[i] : bv[i]);
-            best = tb1 ? mb : m2;
-            bc = tb1 ? 3 : (ta ? 2 : bc);
-          }
-        }
-        // blocks reach this warpgroup in increasing order, so ties keep the older entry
-        const bool need = diag || forced || best * ps > sc[CAP - 1];
-        int arg = 0;
-        if (need && track) {
-          int aa = 31;
-#pragma unroll
-          for (int i = 30; i >= 0; --i) aa = (__uint_as_float(bv[i]) == best) ? i : aa;
-          arg = bc * 32 + aa;
-        }
-        if (last) {  // both blocks of the step read: release the accumulator
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(b_accempty(acc));
-        }
+      for (int c2 = 0; c2 < 2; ++c2) {  // 64 columns per TMEM round trip
+        uint32_t va[32], vb[32];
+        tmem_ld32x2(tb + c2 * 64, tb + c2 * 64 + 32, va, vb);
         if (diag) {
-          dsv = best * ps;
-          dav = ((uint32_t)n << 8) | (uint32_t)arg;
-          handled_diag = true;
-        } else if (forced) {  // kept whatever its score: a slot of its own, not the ranking
-          const int u = (J - n) / a.dilation - 1;
-          f_sc[u * 128 + row] = best * ps;
-          f_id[u * 128 + row] = ((uint32_t)n << 8) | (uint32_t)arg;
-        } else if (need) {
-          list_insert_newer<CAP>(sc, id, best * ps, ((uint32_t)n << 8) | (uint32_t)arg);
+          const uint32_t neg = __float_as_uint(-FLT_MAX);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (c2 * 64 + i > row) va[i] = neg;
+            if (c2 * 64 + 32 + i > row) vb[i] = neg;
+          }
         }
+        const float ma = max32(va), mb = max32(vb);
+        if (c2 == 0) {
+          const bool tb1 = mb > ma;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (track) bv[i] = tb1 ? vb[i] : va[i];
+          best = tb1 ? mb : ma;
+          bc = tb1 ? 1 : 0;
+        } else {
+          const bool ta = ma > best;
+          const float m2 = ta ? ma : best;
+          const bool tb1 = mb > m2;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (track) bv[i] = tb1 ? vb[i] : (ta ? va[i] : bv[i]);
+          best = tb1 ? mb : m2;
+          bc = tb1 ? 3 : (ta ? 2 : bc);
+        }
+      }
+      // blocks reach this warpgroup in increasing order, so ties keep the older entry
+      const bool need = diag || forced || best * ps > sc[CAP - 1];
+      int arg = 0;
+      if (need && track) {
+        int aa = 31;
+#pragma unroll
+        for (int i = 30; i >= 0; --i) aa = (__uint_as_float(bv[i]) == best) ? i : aa;
+        arg = bc * 32 + aa;
+      }
+      // this block's half of the accumulator has been read
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_accempty(acc));
+      if (diag) {
+        dsv = best * ps;
+        dav = ((uint32_t)n << 8) | (uint32_t)arg;
+        handled_diag = true;
+      } else if (forced) {  // kept whatever its score: a slot of its own, not the ranking
+        const int u = (J - n) / a.dilation - 1;
+        f_sc[u * 128 + row] = best * ps;
+        f_id[u * 128 + row] = ((uint32_t)n << 8) | (uint32_t)arg;
+      } else if (need) {
+        list_insert_newer<CAP>(sc, id, best * ps, ((uint32_t)n << 8) | (uint32_t)arg);
       }
     }
-    // ---- merge warpgroup 1's list into warpgroup 0's ----
+    // ---- merge the lists of warpgroups 1 and 2 into warpgroup 0's ----
     if (handled_diag) {
       d_sc[row] = dsv;
       d_id[row] = dav;
     }
-    if (e == 1) {
+    if (e >= 1) {
 #pragma unroll
       for (int i = 0; i < CAP; ++i) {
-        m_sc[i * 128 + row] = sc[i];
-        m_id[i * 128 + row] = id[i];
+        m_sc[((e - 1) * CAP + i) * 128 + row] = sc[i];
+        m_id[((e - 1) * CAP + i) * 128 + row] = id[i];
       }
     }
-    named_bar_sync(1, 256);
+    named_bar_sync(1, 128 * kSelEpiGroups);
     if (e == 0) {
+#pragma unroll 1
+      for (int w = 0; w < kSelEpiGroups - 1; ++w) {
 #pragma unroll
-      for (int i = 0; i < CAP; ++i) {
-        const uint32_t oid = m_id[i * 128 + row];
-        if (oid != 0xFFFFFFFFu) list_insert<CAP>(sc, id, m_sc[i * 128 + row], oid);
+        for (int i = 0; i < CAP; ++i) {
+          const uint32_t oid = m_id[(w * CAP + i) * 128 + row];
+          if (oid != 0xFFFFFFFFu) list_insert<CAP>(sc, id, m_sc[(w * CAP + i) * 128 + row], oid);
+        }
       }
       dsv = d_sc[row];
       dav = d_id[row];
@@ -420,7 +436,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         }
       }
       const int t = qstart + row;
-      if (row < nrows && t < a.T) {
+      // a CTA whose waits gave up leaves the outputs untouched
+      if (row < nrows && t < a.T && !*abort_flag) {
         const size_t base = ((size_t)t * a.hkv + g) * K;
 #pragma unroll
         for (int s = 0; s < kMaxTopK; ++s) {
@@ -451,7 +468,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kSelMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -461,10 +478,19 @@ template <int DP, int CAP, bool ARG, bool WIN>
 cudaError_t launch_sel_t(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
                          const SelArgs& a, cudaStream_t st) {
   using C = SelCfg<DP>;
-  const size_t smem = 1024 + (1 + 2 * kSelStages) * C::kTileBytes + (WIN ? 2 : 1) * CAP * 128 * 8 +
-                      128 * 8 + (2 * kSelStages + 5) * 8 + 16;
-  cudaError_t e = cudaFuncSetAttribute(k_select<DP, CAP, ARG, WIN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = 1024 + (1 + 2 * kSelStages) * C::kTileBytes +
+                      ((kSelEpiGroups - 1) + (WIN ? 1 : 0)) * CAP * 128 * 8 + 128 * 8 +
+                      (2 * kSelStages + 5) * 8 + 16;
+  // The warpgroups' register budgets are drawn from the registers the block
+  // is launched with; a larger sum would leave setmaxnreg.inc waiting.
+  constexpr int kBudget = kSelEpiGroups * 128 * kSelRegsEpi + 128 * kSelRegsCtl;
+  static_assert(kBudget <= 65536, "register budgets exceed the register file");
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, k_select<DP, CAP, ARG, WIN>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * kSelThreads < kBudget) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(k_select<DP, CAP, ARG, WIN>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = s.nb_bound * s.hkv;
   k_select<DP, CAP, ARG, WIN><<<grid, kSelThreads, smem, st>>>(mq, mk, a);
@@ -496,7 +522,7 @@ cudaError_t launch_select(const Shape& s, const int32_t* cu_seqlens, const int32
   if ((e = make_tmap_3d(&mk, k_p, s.dp, s.hkv, s.T, s.dp, 1, 256, sw)) != cudaSuccess) return e;
   SelArgs a{cu_seqlens, cu_blocks, s.ndoc,   s.T,         s.hkv, s.K,
             s.nb_bound, s.window,  s.dilation, s.proxy_scale, sel_idx, sel_score,
-            sel_arg,    plse,      tie,    status};
+            sel_arg,    plse,      tie,    status, s.test_stall_select};
   const int cap = s.K <= 4 ? 4 : (s.K <= 8 ? 8 : 16);
   if (s.dp == 64) {
     if (cap == 4) return launch_sel_a<64, 4>(s, mq, mk, a, with_arg, st);

@@ -69,7 +69,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 msa_status check_params(const msa_params* p, Shape* s) {
   if (!p) return MSA_ERR_INVALID_ARG;
-  if ((p->flags & ~MSA_FLAG_REUSE_REGROUP) != 0) return MSA_ERR_INVALID_ARG;
+  if ((p->flags & ~(MSA_FLAG_REUSE_REGROUP | MSA_FLAG_TEST_STALL_SELECT)) != 0)
+    return MSA_ERR_INVALID_ARG;
   if (p->total_tokens < 0 || p->num_docs < 1 || p->max_seqlen < 0) return MSA_ERR_INVALID_ARG;
   if (p->total_tokens > 0 && (p->max_seqlen < 1 || p->max_seqlen > p->total_tokens))
     return MSA_ERR_INVALID_ARG;
@@ -114,6 +115,7 @@ msa_status check_params(const msa_params* p, Shape* s) {
   s->softmax_scale = p->softmax_scale;
   s->proxy_scale = p->proxy_scale;
   s->kl_weight = p->kl_weight;
+  s->test_stall_select = (p->flags & MSA_FLAG_TEST_STALL_SELECT) != 0;
   return MSA_OK;
 }
 
@@ -147,12 +149,13 @@ Workspace workspace_layout(const Shape& s, WsKind kind) {
     w.ent = take((size_t)s.T * s.hkv * (size_t)(s.K > 1 ? s.K - 1 : 1) * 4);
   }
   if (kind == kWsFwd) {
-    w.o_part = take((size_t)s.qc_tokens * s.hq * s.K * s.d * 4);  // one query chunk
-    w.lse_part = take((size_t)s.qc_tokens * s.hq * s.K * 4);
+    // one query chunk: int16 partial rows, {lse, scale} per row
+    w.o_part = take((size_t)s.qc_tokens * s.hq * s.K * s.d * 2);
+    w.o_meta = take((size_t)s.qc_tokens * s.hq * s.K * 8);
   }
   if (kind == kWsBwd) {
     w.dsum = take((size_t)s.T * s.hq * 4);
-    w.dq_part = take((size_t)s.qc_tokens * s.hq * s.K * s.d * 4);  // one query chunk
+    w.dq_part = take((size_t)s.qc_tokens * s.hq * s.K * s.d * 4);  // one query chunk, fp32
     w.kl_part = take((size_t)bwd_reduce_blocks(s) * 8 + 8);
     // one record per list entry (diagonal + gathered) of every (group, block),
     // plus one tile of padding read by the last tile's bulk copy
@@ -274,8 +277,8 @@ msa_status msa_fwd(const msa_params* p, const int32_t* cu_seqlens, const uint16_
   uint32_t* cnt = reinterpret_cast<uint32_t*>(base + w.cnt);
   int32_t* row_ptr = reinterpret_cast<int32_t*>(base + w.row_ptr);
   uint32_t* ent = reinterpret_cast<uint32_t*>(base + w.ent);
-  float* o_part = reinterpret_cast<float*>(base + w.o_part);
-  float* lse_part = reinterpret_cast<float*>(base + w.lse_part);
+  int16_t* o_part = reinterpret_cast<int16_t*>(base + w.o_part);
+  float2* o_meta = reinterpret_cast<float2*>(base + w.o_meta);
   const bool reuse = (p->flags & MSA_FLAG_REUSE_REGROUP) != 0;
   if (!reuse) {
     MSA_TRY(launch_meta(s, cu_seqlens, cu_blocks, status, cs));
@@ -287,10 +290,10 @@ msa_status msa_fwd(const msa_params* p, const int32_t* cu_seqlens, const uint16_
   const int nq = s.nqchunks;
   for (int c = 0; c < nq; ++c) {
     const int chunk = nq == 1 ? -1 : c;
-    MSA_TRY(launch_fwd(s, cu_seqlens, cu_blocks, row_ptr, ent, q, k, v, o_part, lse_part, chunk,
+    MSA_TRY(launch_fwd(s, cu_seqlens, cu_blocks, row_ptr, ent, q, k, v, o_part, o_meta, chunk,
                        status, cs));
     if (c == nq - 1) MSA_TRY(prof_mark(2, false, cs));
-    MSA_TRY(launch_fwd_merge(s, cu_seqlens, cu_blocks, o_part, lse_part, o, o_res, lse, mass,
+    MSA_TRY(launch_fwd_merge(s, cu_seqlens, cu_blocks, o_part, o_meta, o, o_res, lse, mass,
                              chunk, cs));
   }
   g_launches += (reuse ? 0 : 5) + 2 * nq;

@@ -77,6 +77,33 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
+// ---------------------------------------------------------------------------
+// 16-bit fixed-point slot partials of the forward.  The normalised O of one
+// (token, head, slot) is stored as int16 values q = rint(x * 32767 / m),
+// m = max |x| over the row (one thread owns the row), with the fp32 scale
+// m / 32767 beside it; the merge adds scale * q.  |x| <= m makes |q| <= 32767,
+// and the error is at most m / 65534 per element: about 16 bits of the row's
+// largest value, which the backward's D = rowsum(dO * O) needs (bf16, 8 bits,
+// or fp16, 11 bits, partials are not enough).  The backward's dQ partials stay
+// fp32: there one warp holds a row one element per lane, and the per-row
+// maximum would take a cross-lane reduction per row.
+// ---------------------------------------------------------------------------
+constexpr float kQ16 = 32767.f;
+// Magnitude bits of an fp32 value: for non-negative floats the integer order
+// of the bits is the numeric order, so an integer max gives max |x| exactly.
+__device__ __forceinline__ uint32_t abs_bits(uint32_t x) { return x & 0x7FFFFFFFu; }
+// 32767 / m, or 0 for an all-zero row.
+__device__ __forceinline__ float q16_factor(float m) { return m > 0.f ? __fdividef(kQ16, m) : 0.f; }
+// a and b rounded to the nearest integer, packed as int16 with a in the low half.
+__device__ __forceinline__ uint32_t pack_q16x2(float a, float b) {
+  const int ia = __float2int_rn(a), ib = __float2int_rn(b);
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(d) : "r"(ia), "r"(ib));
+  return d;
+}
+__device__ __forceinline__ float q16_lo(uint32_t x) { return (float)(int)(int16_t)(x & 0xFFFFu); }
+__device__ __forceinline__ float q16_hi(uint32_t x) { return (float)((int)x >> 16); }
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -124,11 +151,12 @@ struct Shape {
   int qc_blocks; // KV blocks per query chunk (qchunk_of)
   int nqchunks;  // query chunks of the slot partials
   int qc_tokens; // tokens of the largest query chunk: rows of the partial buffers
+  bool test_stall_select;  // MSA_FLAG_TEST_STALL_SELECT
 };
 
 // ---------------------------------------------------------------------------
 // Query chunks.  The per-slot partials of the forward (O, lse) and backward
-// (dQ) take T * Hq * k * d * 4 bytes each; to bound the workspace, one call
+// (dQ) take T * Hq * k * d * 2 and 4 bytes; to bound the workspace, one call
 // processes the queries in chunks of whole KV blocks: chunk c holds the
 // queries of global blocks [c * qcb, (c + 1) * qcb), so at most qcb * 128
 // tokens (qcb = kQChunkBlocks unless the environment variable
@@ -175,8 +203,8 @@ __device__ __forceinline__ int lower_bound_token(const uint32_t* ent, int lo, in
 // Workspace carve-up (byte offsets, 256-byte aligned).
 struct Workspace {
   size_t cu_blocks, chunk_range, cnt, row_ptr, ent;          // metadata + regroup CSR
-  size_t o_part, lse_part;                                     // forward slot partials
-  size_t dsum, dq_part, kl_part, rec;                          // backward
+  size_t o_part, o_meta;                  // forward slot partials: int16 rows, {lse, scale}
+  size_t dsum, dq_part, kl_part, rec;     // backward (dQ partials fp32)
   size_t total;
 };
 enum WsKind { kWsSelect = 0, kWsFwd = 1, kWsBwd = 2 };
@@ -214,10 +242,10 @@ cudaError_t launch_regroup(const Shape& s, const int32_t* cu_seqlens, const int3
                            int32_t* row_ptr, uint32_t* ent, unsigned* status, cudaStream_t st);
 cudaError_t launch_fwd(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
                        const int32_t* row_ptr, const uint32_t* ent, const uint16_t* q,
-                       const uint16_t* k, const uint16_t* v, float* o_part, float* lse_part,
+                       const uint16_t* k, const uint16_t* v, int16_t* o_part, float2* o_meta,
                        int chunk, unsigned* status, cudaStream_t st);
 cudaError_t launch_fwd_merge(const Shape& s, const int32_t* cu_seqlens, const int32_t* cu_blocks,
-                             const float* o_part, const float* lse_part, uint16_t* o,
+                             const int16_t* o_part, const float2* o_meta, uint16_t* o,
                              uint16_t* o_res, float* lse, float* mass, int chunk,
                              cudaStream_t st);  // chunk as launch_bwd_reduce
 cudaError_t launch_bwd_pre(const Shape& s, const uint16_t* o, const uint16_t* o_res,

@@ -120,7 +120,8 @@ typedef struct msa_params {
   float softmax_scale;  /* multiplies q . k (1.0 when q is pre-scaled) */
   float proxy_scale;    /* multiplies q_p . k_p (1.0 when q_p is pre-scaled) */
   float kl_weight;      /* lambda of the proxy KL loss */
-  uint32_t flags;       /* 0 or MSA_FLAG_REUSE_REGROUP; other bits are rejected */
+  uint32_t flags;       /* MSA_FLAG_REUSE_REGROUP, MSA_FLAG_TEST_STALL_SELECT or 0; other bits
+                           are rejected */
 } msa_params;
 
 /*
@@ -136,6 +137,21 @@ typedef struct msa_params {
  * not hold, the results are undefined.
  */
 #define MSA_FLAG_REUSE_REGROUP 0x1u
+
+/*
+ * Test hook for the failure path (no use in training).  msa_proxy_select's
+ * scoring kernel withholds the load of its query tile, so the wait of its MMA
+ * warp on that load (or the epilogue's wait on the first scores, whichever
+ * gives up first) runs out after the bounded-wait limit (about half a second
+ * of SM cycles).  Every CTA then records MSA_ERR_TIMEOUT in the device status
+ * word (kernel 1, see msa_last_status_word), lets the copies it did issue
+ * land, frees its tensor memory and returns without writing its outputs:
+ * sel_idx, sel_score, plse and tie keep their previous contents, and the rest
+ * of the call (block lists, argmax offsets) runs on them.  The GPU stays
+ * usable; the next call without the flag is unaffected.  msa_fwd and msa_bwd
+ * ignore the flag.
+ */
+#define MSA_FLAG_TEST_STALL_SELECT 0x100u
 
 typedef enum msa_status {
   MSA_OK = 0,

@@ -60,6 +60,11 @@ def test_workspace_sizes_and_shape_checks(m):
         assert m.msa_fwd_workspace_size(bad) == 0
     reuse = m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4, flags=m.MSA_FLAG_REUSE_REGROUP)
     assert m.msa_bwd_workspace_size(reuse) == m.msa_bwd_workspace_size(ok)
+    stall = m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4, flags=m.MSA_FLAG_TEST_STALL_SELECT)
+    assert m.msa_select_workspace_size(stall) == m.msa_select_workspace_size(ok)
+    both = m.MSA_FLAG_TEST_STALL_SELECT | m.MSA_FLAG_REUSE_REGROUP | 0x200  # one unknown bit
+    assert m.msa_select_workspace_size(m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4,
+                                                     flags=both)) == 0
 
 
 def _call_fwd(m, prm, ptr_val, ws_bytes):
