@@ -38,12 +38,16 @@
 namespace msa {
 namespace {
 
-constexpr int kSelStages = 4;  // k_p ring stages, two key blocks each
 constexpr int kSelThreads = 512;
 constexpr int kSelEpiGroups = 3;
 constexpr int kSelProducerWarp = 12, kSelMmaWarp = 13;
 constexpr uint32_t kSelRegsEpi = 152, kSelRegsCtl = 56;
 constexpr float kTieBand = 1e-3f;
+
+// k_p ring stages (two key blocks each).  The TMA latency of a stage is about
+// 3000 SM cycles at 128k, three steps' worth; six stages measured no faster.
+template <bool WIN>
+constexpr int sel_stages() { return 4; }
 
 template <int DP>
 struct SelCfg {
@@ -135,29 +139,34 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     k_select(const __grid_constant__ CUtensorMap tm_qp, const __grid_constant__ CUtensorMap tm_kp,
              const SelArgs a) {
   using C = SelCfg<DP>;
+  constexpr int kSelStages = sel_stages<WIN>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   // ---- shared memory carve-up ----
   uint8_t* sQ = smem;                                   // q_p tile, 128 rows
   uint8_t* sK = sQ + C::kTileBytes;                     // k_p ring: pairs of 128-key blocks
-  // lists of warpgroups 1 and 2 for the merge: [2][CAP][128]
-  float* m_sc = reinterpret_cast<float*>(sK + kSelStages * 2 * C::kTileBytes);
+  // lists of warpgroups 1 and 2 for the merge, [2][CAP][128]: in the k_p ring,
+  // which is free by then
+  float* m_sc = reinterpret_cast<float*>(sK);
   uint32_t* m_id = reinterpret_cast<uint32_t*>(m_sc + 2 * CAP * 128);
-  float* d_sc = reinterpret_cast<float*>(m_id + 2 * CAP * 128);             // [128]
+  static_assert(2 * CAP * 128 * 8 <= kSelStages * 2 * C::kTileBytes, "merge lists fit the ring");
+  float* d_sc = reinterpret_cast<float*>(sK + kSelStages * 2 * C::kTileBytes);  // [128]
   uint32_t* d_id = reinterpret_cast<uint32_t*>(d_sc + 128);                 // [128]
   // [CAP][128] always-kept blocks (block pattern only)
   float* f_sc = reinterpret_cast<float*>(d_id + 128);
   uint32_t* f_id = reinterpret_cast<uint32_t*>(f_sc + (WIN ? CAP * 128 : 0));
   uint64_t* bars = reinterpret_cast<uint64_t*>(f_id + (WIN ? CAP * 128 : 0));
   // bars: 0 qfull | 1..S kvfull | S+1..2S kvempty | 2S+1..2S+2 accfull | 2S+3..2S+4 accempty
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kSelStages + 5);
+  // | 2S+5 MMAs done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kSelStages + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   const uint32_t b_qfull = smem_u32(bars);
   auto b_kvfull = [&](int s) { return smem_u32(bars + 1 + s); };
   auto b_kvempty = [&](int s) { return smem_u32(bars + 1 + kSelStages + s); };
   auto b_accfull = [&](int i) { return smem_u32(bars + 1 + 2 * kSelStages + i); };
   auto b_accempty = [&](int i) { return smem_u32(bars + 3 + 2 * kSelStages + i); };
+  const uint32_t b_mmadone = smem_u32(bars + 5 + 2 * kSelStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -186,6 +195,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       mbar_init(b_accfull(i), 1);
       mbar_init(b_accempty(i), 8);  // four warps for each of the step's two blocks
     }
+    mbar_init(b_mmadone, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -256,6 +266,9 @@ __global__ void __launch_bounds__(kSelThreads, 1)
             umma_commit(b_accfull(acc));
           }
         }
+        // every MMA issued by this CTA completes before TMEM is released
+        umma_commit(b_mmadone);
+        drain_bar(b_mmadone, 0);
       }
     }
   } else {
@@ -308,6 +321,11 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       for (int c2 = 0; c2 < 2; ++c2) {  // 64 columns per TMEM round trip
         uint32_t va[32], vb[32];
         tmem_ld32x2(tb + c2 * 64, tb + c2 * 64 + 32, va, vb);
+        if (c2 == 1) {  // the block's scores are all in registers: release its accumulator half
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_accempty(acc));
+        }
         if (diag) {
           const uint32_t neg = __float_as_uint(-FLT_MAX);
 #pragma unroll
@@ -344,10 +362,6 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         for (int i = 30; i >= 0; --i) aa = (__uint_as_float(bv[i]) == best) ? i : aa;
         arg = bc * 32 + aa;
       }
-      // this block's half of the accumulator has been read
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_accempty(acc));
       if (diag) {
         dsv = best * ps;
         dav = ((uint32_t)n << 8) | (uint32_t)arg;
@@ -365,6 +379,9 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       d_sc[row] = dsv;
       d_id[row] = dav;
     }
+    // every warpgroup has read its last scores: every MMA and so every k_p
+    // load has completed, and the lists can go into the ring
+    named_bar_sync(1, 128 * kSelEpiGroups);
     if (e >= 1) {
 #pragma unroll
       for (int i = 0; i < CAP; ++i) {
@@ -478,9 +495,12 @@ template <int DP, int CAP, bool ARG, bool WIN>
 cudaError_t launch_sel_t(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
                          const SelArgs& a, cudaStream_t st) {
   using C = SelCfg<DP>;
-  const size_t smem = 1024 + (1 + 2 * kSelStages) * C::kTileBytes +
-                      ((kSelEpiGroups - 1) + (WIN ? 1 : 0)) * CAP * 128 * 8 + 128 * 8 +
-                      (2 * kSelStages + 5) * 8 + 16;
+  constexpr int kSelStages = sel_stages<WIN>();
+  const size_t smem = 1024 + (1 + 2 * kSelStages) * C::kTileBytes + (WIN ? CAP * 128 * 8 : 0) +
+                      128 * 8 + (2 * kSelStages + 6) * 8 + 16;
+  static_assert(1024 + (1 + 2 * kSelStages) * SelCfg<64>::kTileBytes + (WIN ? 16 * 128 * 8 : 0) +
+                        128 * 8 + (2 * kSelStages + 6) * 8 + 16 <= 232448,
+                "shared memory budget");
   // The warpgroups' register budgets are drawn from the registers the block
   // is launched with; a larger sum would leave setmaxnreg.inc waiting.
   constexpr int kBudget = kSelEpiGroups * 128 * kSelRegsEpi + 128 * kSelRegsCtl;

@@ -22,7 +22,7 @@ KERNEL_SELECT = 1
 # barriers of the selection kernel a stalled CTA can give up on: the query
 # tile (MMA warp), the k_p ring stages (producer) and the two score
 # accumulators (epilogue)
-SELECT_WAITS = {0, 7, 8, 9, 10, 13, 14}
+SELECT_WAITS = {0, 7, 8, 9, 10, 11, 12, 13, 14}
 
 
 def test_select_wait_that_runs_out_reports_timeout_and_next_call_is_clean():
