@@ -8,6 +8,7 @@ through the C ABI of libmsa.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 128k|512k|1m|varlen|tiny]
                     [--impl ours|reference] [--no-dense] [--no-cpu-baseline] [--no-configs]
+                    [--only-select]
 
 Prints one JSON line (rank 0).  `value` is the effective TFLOP/s of the step
 on the headline workload (128k tokens unless --workload says otherwise):
@@ -467,6 +468,50 @@ def measure_config(name, peaks, args, cpu_rows, dense_steps, K, W, world=1) -> d
     return rec
 
 
+def run_select_only(args):
+    """The selection call alone on the workload's inputs, for profiling: only
+    cu_seqlens, q_p, k_p, the selection outputs and the selection workspace
+    stay on the device.  Prints one JSON line with the call's time."""
+    import block_sparse_attention_proxy_gb300 as m
+    from block_sparse_attention_proxy_gb300.step import params_for
+
+    dist_setup()
+    m.load()
+    w = synth.workload(args.workload)
+    inp = make_device_inputs(w)
+    cu, qp, kp = inp["cu_seqlens"], inp["q_p"], inp["k_p"]
+    del inp
+    torch.cuda.empty_cache()
+    prm = params_for(cu.tolist(), w.hq, w.hkv, w.d, w.dp, w.top_k)
+    T, hkv, K = w.total_tokens, w.hkv, w.top_k
+    out = dict(sel_idx=torch.empty(T, hkv, K, dtype=torch.int32, device="cuda"),
+               sel_score=torch.empty(T, hkv, K, dtype=torch.float32, device="cuda"),
+               sel_arg=torch.empty(T, hkv, K, dtype=torch.uint8, device="cuda"),
+               plse=torch.empty(T, hkv, dtype=torch.float32, device="cuda"),
+               tie=torch.empty(T, hkv, dtype=torch.uint8, device="cuda"))
+    ws = m.workspace(m.msa_select_workspace_size(prm))
+
+    def call():
+        m.msa_proxy_select(prm, cu, qp, kp, out["sel_idx"], out["sel_score"], out["sel_arg"],
+                           out["plse"], out["tie"], ws)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    if m.msa_get_device_status() != 0:
+        raise RuntimeError(f"device status {m.msa_last_status_word():#x}")
+    print(json.dumps(dict(workload=w.name, call="msa_proxy_select", steps=args.steps,
+                          ms_per_call=round(e0.elapsed_time(e1) / max(1, args.steps), 3),
+                          device_peak_gb=round(torch.cuda.max_memory_allocated() / 1e9, 2))),
+          flush=True)
+
+
 def run_ours(args):
     import block_sparse_attention_proxy_gb300 as m
     from block_sparse_attention_proxy_gb300.step import MSAStep, params_for
@@ -719,6 +764,8 @@ def main():
                          "(per_config records); default: the whole range")
     ap.add_argument("--no-configs", dest="configs", action="store_const", const="",
                     help="measure only the headline workload (no per_config records)")
+    ap.add_argument("--only-select", action="store_true",
+                    help="profiling: time the selection call alone (few GB on the device)")
     ap.add_argument("--cpu-rows", type=int, default=128)
     ap.add_argument("--ref-rows", type=int, default=4)
     args = ap.parse_args()
@@ -726,6 +773,8 @@ def main():
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args)
+    elif args.only_select:
+        run_select_only(args)
     else:
         run_ours(args)
 
