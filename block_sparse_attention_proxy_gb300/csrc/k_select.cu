@@ -170,26 +170,39 @@ __global__ void __launch_bounds__(kSelThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item: query block J of document d, group g (heaviest first) ----
-  if (!a.cu_blocks[a.ndoc + 1]) return;  // malformed cu_seqlens (flagged by k_meta)
+  // ---- work item.  A cluster of two CTAs takes query blocks gb0 and gb0 - 1
+  // of group g (heaviest first); CTA `rank` takes gb0 - rank.  When both lie
+  // in one document (paired), their key blocks 0..J-1 are the same k_p rows:
+  // each CTA loads one of the two key blocks of a step and multicasts it to
+  // both, so the pair reads k_p from L2 once instead of twice. ----
+  const uint32_t rank = cluster_ctarank();
+  const bool ok_batch = a.cu_blocks[a.ndoc + 1] != 0;  // else malformed cu_seqlens (flagged by k_meta)
   const int nbt = min(a.cu_blocks[a.ndoc], a.nb_bound);
-  const int g = blockIdx.x % a.hkv;
-  const int gb = nbt - 1 - (int)(blockIdx.x / a.hkv);
-  if (gb < 0) return;
-  const int d = doc_of_block(a.cu_blocks, a.ndoc, gb);
-  const int J = gb - a.cu_blocks[d];
-  const int dstart = a.cu[d];
-  const int L = a.cu[d + 1] - dstart;
+  const int cl = (int)(blockIdx.x >> 1);
+  const int g = cl % a.hkv;
+  const int gb0 = nbt - 1 - 2 * (cl / a.hkv);
+  const int gb = gb0 - (int)rank;
+  const bool has = ok_batch && gb >= 0;  // warp- and CTA-uniform
+  const bool paired = ok_batch && gb0 >= 1 &&
+                      doc_of_block(a.cu_blocks, a.ndoc, gb0) == doc_of_block(a.cu_blocks, a.ndoc, gb0 - 1);
+  const int d = has ? doc_of_block(a.cu_blocks, a.ndoc, gb) : 0;
+  const int J = has ? gb - a.cu_blocks[d] : 0;
+  const int dstart = has ? a.cu[d] : 0;
+  const int L = has ? a.cu[d + 1] - dstart : 0;
   const int qstart = dstart + J * kBlock;
   const int nrows = min(kBlock, L - J * kBlock);
-  const int nblk = J + 1;
+  const int nblk = has ? J + 1 : 0;
   const int nstep = (nblk + 1) / 2;  // steps of two key blocks (the last may hold one)
+  // Steps both CTAs of a pair take (rank 1's count; rank 0 may have one more,
+  // which it loads alone); 0 when not paired.
+  const int common = paired ? (J - (int)(rank == 0) + 2) / 2 : 0;
+  constexpr uint16_t kPair = 0x3;
 
   if (threadIdx.x == 0) {
     mbar_init(b_qfull, 1);
     for (int s = 0; s < kSelStages; ++s) {
       mbar_init(b_kvfull(s), 1);
-      mbar_init(b_kvempty(s), 1);
+      mbar_init(b_kvempty(s), paired ? 2 : 1);  // a paired stage is released by both MMA warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_accfull(i), 1);
@@ -199,16 +212,21 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kSelMmaWarp) {
+  if (has && warp == kSelMmaWarp) {
     tmem_alloc(smem_u32(tslot), 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(tslot);
+  // the peer's barriers are initialised before any multicast copy or commit
+  // reaches them
+  cluster_sync();
+  const uint32_t tbase = has ? *reinterpret_cast<volatile uint32_t*>(tslot) : 0u;
 
-  if (warp >= 4 * kSelEpiGroups) {
+  if (!has) {
+    // no query block for this CTA: nothing but the cluster barrier below
+  } else if (warp >= 4 * kSelEpiGroups) {
     setmaxnreg_dec<kSelRegsCtl>();
     if (warp == kSelProducerWarp) {
       // ------------------------------ TMA producer ------------------------------
@@ -229,8 +247,15 @@ __global__ void __launch_bounds__(kSelThreads, 1)
                         wait_site(kKerSelect, 7 + s, m)))
             break;
           mbar_arrive_expect_tx(b_kvfull(s), 2 * C::kTileBytes);
-          tma_load_3d(smem_u32(sK + s * 2 * C::kTileBytes), &tm_kp, b_kvfull(s), 0, g,
-                      dstart + 2 * m * kBlock);
+          const uint32_t dst = smem_u32(sK + s * 2 * C::kTileBytes);
+          if (m < common) {  // this CTA's key block of the step, for both CTAs
+            tma_load_3d_mc(dst + rank * C::kTileBytes, &tm_kp, b_kvfull(s), 0, g,
+                           dstart + (2 * m + (int)rank) * kBlock, kPair);
+          } else {
+            tma_load_3d(dst, &tm_kp, b_kvfull(s), 0, g, dstart + 2 * m * kBlock);
+            tma_load_3d(dst + C::kTileBytes, &tm_kp, b_kvfull(s), 0, g,
+                        dstart + (2 * m + 1) * kBlock);
+          }
           issued = m + 1;
         }
         // Let this CTA's own copies land before it exits (they have, unless a
@@ -262,7 +287,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
               const uint64_t bd = make_sdesc(k0 + kk * 32, 16, C::kSBO, C::kLayout);
               umma_bf16(tbase + acc * 256, ad, bd, idesc, kk > 0);
             }
-            umma_commit(b_kvempty(s));
+            if (m < common) umma_commit_mc(b_kvempty(s), kPair);  // both CTAs' copies of the stage
+            else umma_commit(b_kvempty(s));
             umma_commit(b_accfull(acc));
           }
         }
@@ -485,10 +511,13 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kSelMmaWarp) {
+  if (has && warp == kSelMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  // neither CTA leaves while the other may still copy into its shared memory
+  // or arrive on its barriers
+  cluster_sync();
 }
 
 template <int DP, int CAP, bool ARG, bool WIN>
@@ -512,8 +541,21 @@ cudaError_t launch_sel_t(const Shape& s, const CUtensorMap& mq, const CUtensorMa
   e = cudaFuncSetAttribute(k_select<DP, CAP, ARG, WIN>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int grid = s.nb_bound * s.hkv;
-  k_select<DP, CAP, ARG, WIN><<<grid, kSelThreads, smem, st>>>(mq, mk, a);
+  // clusters of two CTAs: query blocks gb0 and gb0 - 1 of one group
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * s.hkv * ((s.nb_bound + 1) / 2)));
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_select<DP, CAP, ARG, WIN>, mq, mk, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -539,7 +581,8 @@ cudaError_t launch_select(const Shape& s, const int32_t* cu_seqlens, const int32
   const int sw = s.dp == 64 ? 128 : 64;
   cudaError_t e;
   if ((e = make_tmap_3d(&mq, q_p, s.dp, s.hkv, s.T, s.dp, 1, 128, sw)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&mk, k_p, s.dp, s.hkv, s.T, s.dp, 1, 256, sw)) != cudaSuccess) return e;
+  // one 128-row key block per box (a step loads two, or one per CTA of a pair)
+  if ((e = make_tmap_3d(&mk, k_p, s.dp, s.hkv, s.T, s.dp, 1, 128, sw)) != cudaSuccess) return e;
   SelArgs a{cu_seqlens, cu_blocks, s.ndoc,   s.T,         s.hkv, s.K,
             s.nb_bound, s.window,  s.dilation, s.proxy_scale, sel_idx, sel_score,
             sel_arg,    plse,      tie,    status, s.test_stall_select};
