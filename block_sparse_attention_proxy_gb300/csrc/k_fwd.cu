@@ -17,11 +17,14 @@
 // point relative to the row's max |O_slot| (int16 row + fp32 scale, beside
 // lse_slot); the merge kernel combines the slots by log-sum-exp.
 //
-// Roles (320 threads): two softmax warpgroups (warps 0-3 and 4-7) take
+// Roles (384 threads): two softmax warpgroups (warps 0-3 and 4-7) take
 // alternate tiles through two S/O accumulator pairs, so one warpgroup's
 // softmax overlaps the other's P V product and O stores; warp 8 is the TMA
 // producer (regroup entries read one tile ahead, three Q stages); warp 9 issues
-// the MMAs.
+// the MMAs; warps 10-11 only complete the third warpgroup, so that register
+// budgets can be set per warpgroup (setmaxnreg): 2 x 128 x 200 for the softmax
+// warps, 128 x 104 for the producer and MMA warps, 64512 = 384 x 168 in all (at
+// 320 threads every warp was capped at 168 and the softmax warps spilled).
 #include <cfloat>
 
 #include "msa_internal.cuh"
@@ -29,7 +32,8 @@
 namespace msa {
 namespace {
 
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 384;
+constexpr uint32_t kFwdRegsSoftmax = 200, kFwdRegsCtl = 104;
 constexpr int kFwdQStages = 3;
 // Per softmax warp: a 32-row x 64-column int16 staging tile (128B-swizzled
 // rows) and the 32 row pointers, used to turn row-per-thread O values into
@@ -167,102 +171,106 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     return t < a.T;
   };
 
-  if (warp == 8) {
-    // ------------------------------ TMA producer ------------------------------
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(B_KV), 2 * kTile);
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        tma_load_3d(smem_u32(sK + c * 16384), &tm_k, bar(B_KV), 64 * c, g, kstart);
-        tma_load_3d(smem_u32(sV + c * 16384), &tm_v, bar(B_KV), 64 * c, g, kstart);
-      }
-    }
-    int tok[TPL];
-    auto load_tokens = [&](int n) {
-#pragma unroll
-      for (int u = 0; u < TPL; ++u) {
-        const int i = lane + 32 * u;
-        int t = a.T, slot;
-        if (i < TPT && !tile_token(n, i, t, slot)) t = a.T;
-        tok[u] = t;
-      }
-    };
-    if (ntiles > 0) load_tokens(0);
-    for (int n = 0; n < ntiles; ++n) {
-      const int s = n % NQ;
-      if (n >= NQ && !wait_bar_warp(bar(B_QE + s), ((n / NQ) & 1) ^ 1, abort_flag, a.status,
-                                    wait_site(kKerFwd, B_QE + s, n)))
-        break;
-      int cur[TPL];
-#pragma unroll
-      for (int u = 0; u < TPL; ++u) cur[u] = tok[u];
-      if (n + 1 < ntiles) load_tokens(n + 1);
-      if (lane == 0) mbar_arrive_expect_tx(bar(B_QF + s), kTile);
-      __syncwarp();
-      const uint32_t qb = smem_u32(sQ + s * kTile);
-#pragma unroll
-      for (int u = 0; u < TPL; ++u) {
-        const int i = lane + 32 * u;
-        if (i < TPT) {
-#pragma unroll
-          for (int c = 0; c < NCH; ++c)
-            tma_load_3d(qb + c * 16384 + i * G * 128, &tm_q, bar(B_QF + s), 64 * c, g * G, cur[u]);
+  if (warp >= 8) {
+    setmaxnreg_dec<kFwdRegsCtl>();
+    if (warp == 8) {
+      // ------------------------------ TMA producer ------------------------------
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(B_KV), 2 * kTile);
+  #pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          tma_load_3d(smem_u32(sK + c * 16384), &tm_k, bar(B_KV), 64 * c, g, kstart);
+          tma_load_3d(smem_u32(sV + c * 16384), &tm_v, bar(B_KV), 64 * c, g, kstart);
         }
       }
-    }
-  } else if (warp == 9) {
-    // ------------------------------ MMA issuer ---------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idO = make_idesc_bf16(128, D, false, true);
-      bool ok = wait_bar(bar(B_KV), 0, abort_flag, a.status, wait_site(kKerFwd, B_KV, 0));
-      const uint32_t k0 = smem_u32(sK), v0 = smem_u32(sV);
-      auto issue_s = [&](int n) -> bool {
-        const int s = n % NQ, b = n & 1;
-        if (!wait_bar(bar(B_QF + s), (n / NQ) & 1, abort_flag, a.status,
-                      wait_site(kKerFwd, B_QF + s, n)))
-          return false;
-        // S(n) overwrites the P of tile n-2: wait until that P V has completed
-        if (n >= 2 && !wait_bar(bar(b_ofull(b)), ((n - 2) >> 1) & 1, abort_flag, a.status,
-                                wait_site(kKerFwd, b_ofull(b), n)))
-          return false;
-        tc_fence_after();
-        const uint32_t q0 = smem_u32(sQ + s * kTile);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16(tbase + 128 * b, make_sdesc(q0 + off, 16, 1024, kLayoutSW128),
-                    make_sdesc(k0 + off, 16, 1024, kLayoutSW128), idS, kk > 0);
+      int tok[TPL];
+      auto load_tokens = [&](int n) {
+  #pragma unroll
+        for (int u = 0; u < TPL; ++u) {
+          const int i = lane + 32 * u;
+          int t = a.T, slot;
+          if (i < TPT && !tile_token(n, i, t, slot)) t = a.T;
+          tok[u] = t;
         }
-        umma_commit(bar(b_sfull(b)));
-        umma_commit(bar(B_QE + s));
-        return true;
       };
-      if (ok && ntiles > 0) ok = issue_s(0);
-      for (int n = 1; ok && n <= ntiles; ++n) {
-        // P V for tile n-1, then S for tile n
-        const int m = n - 1, b = m & 1;
-        if (!wait_bar(bar(b_pfull(b)), (m >> 1) & 1, abort_flag, a.status,
-                      wait_site(kKerFwd, b_pfull(b), m)))
+      if (ntiles > 0) load_tokens(0);
+      for (int n = 0; n < ntiles; ++n) {
+        const int s = n % NQ;
+        if (n >= NQ && !wait_bar_warp(bar(B_QE + s), ((n / NQ) & 1) ^ 1, abort_flag, a.status,
+                                      wait_site(kKerFwd, B_QE + s, n)))
           break;
-        if (m >= 2 && !wait_bar(bar(b_oempty(b)), ((m >> 1) & 1) ^ 1, abort_flag, a.status,
-                                wait_site(kKerFwd, b_oempty(b), m)))
-          break;
-        tc_fence_after();
-        const uint32_t pa = tbase + 128 * b;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // keys 16kk..16kk+15: hi at column 32(kk/2) + 8(kk%2), lo 16 columns further
-          const uint32_t ph = pa + 32 * (kk >> 1) + 8 * (kk & 1);
-          const uint64_t bd = make_sdesc(v0 + kk * 2048, 16384, 1024, kLayoutSW128);
-          umma_bf16_ts(tbase + 256 + b * D, ph, bd, idO, kk > 0);
-          umma_bf16_ts(tbase + 256 + b * D, ph + 16, bd, idO, 1u);
+        int cur[TPL];
+  #pragma unroll
+        for (int u = 0; u < TPL; ++u) cur[u] = tok[u];
+        if (n + 1 < ntiles) load_tokens(n + 1);
+        if (lane == 0) mbar_arrive_expect_tx(bar(B_QF + s), kTile);
+        __syncwarp();
+        const uint32_t qb = smem_u32(sQ + s * kTile);
+  #pragma unroll
+        for (int u = 0; u < TPL; ++u) {
+          const int i = lane + 32 * u;
+          if (i < TPT) {
+  #pragma unroll
+            for (int c = 0; c < NCH; ++c)
+              tma_load_3d(qb + c * 16384 + i * G * 128, &tm_q, bar(B_QF + s), 64 * c, g * G, cur[u]);
+          }
         }
-        umma_commit(bar(b_ofull(b)));
-        if (n < ntiles && !issue_s(n)) break;
+      }
+    } else if (warp == 9) {
+      // ------------------------------ MMA issuer ---------------------------------
+      if (lane == 0) {
+        constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
+        constexpr uint32_t idO = make_idesc_bf16(128, D, false, true);
+        bool ok = wait_bar(bar(B_KV), 0, abort_flag, a.status, wait_site(kKerFwd, B_KV, 0));
+        const uint32_t k0 = smem_u32(sK), v0 = smem_u32(sV);
+        auto issue_s = [&](int n) -> bool {
+          const int s = n % NQ, b = n & 1;
+          if (!wait_bar(bar(B_QF + s), (n / NQ) & 1, abort_flag, a.status,
+                        wait_site(kKerFwd, B_QF + s, n)))
+            return false;
+          // S(n) overwrites the P of tile n-2: wait until that P V has completed
+          if (n >= 2 && !wait_bar(bar(b_ofull(b)), ((n - 2) >> 1) & 1, abort_flag, a.status,
+                                  wait_site(kKerFwd, b_ofull(b), n)))
+            return false;
+          tc_fence_after();
+          const uint32_t q0 = smem_u32(sQ + s * kTile);
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_bf16(tbase + 128 * b, make_sdesc(q0 + off, 16, 1024, kLayoutSW128),
+                      make_sdesc(k0 + off, 16, 1024, kLayoutSW128), idS, kk > 0);
+          }
+          umma_commit(bar(b_sfull(b)));
+          umma_commit(bar(B_QE + s));
+          return true;
+        };
+        if (ok && ntiles > 0) ok = issue_s(0);
+        for (int n = 1; ok && n <= ntiles; ++n) {
+          // P V for tile n-1, then S for tile n
+          const int m = n - 1, b = m & 1;
+          if (!wait_bar(bar(b_pfull(b)), (m >> 1) & 1, abort_flag, a.status,
+                        wait_site(kKerFwd, b_pfull(b), m)))
+            break;
+          if (m >= 2 && !wait_bar(bar(b_oempty(b)), ((m >> 1) & 1) ^ 1, abort_flag, a.status,
+                                  wait_site(kKerFwd, b_oempty(b), m)))
+            break;
+          tc_fence_after();
+          const uint32_t pa = tbase + 128 * b;
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // keys 16kk..16kk+15: hi at column 32(kk/2) + 8(kk%2), lo 16 columns further
+            const uint32_t ph = pa + 32 * (kk >> 1) + 8 * (kk & 1);
+            const uint64_t bd = make_sdesc(v0 + kk * 2048, 16384, 1024, kLayoutSW128);
+            umma_bf16_ts(tbase + 256 + b * D, ph, bd, idO, kk > 0);
+            umma_bf16_ts(tbase + 256 + b * D, ph + 16, bd, idO, 1u);
+          }
+          umma_commit(bar(b_ofull(b)));
+          if (n < ntiles && !issue_s(n)) break;
+        }
       }
     }
   } else {
+    setmaxnreg_inc<kFwdRegsSoftmax>();
     // ------------------------------ softmax / epilogue --------------------------
     // Warpgroup e takes tiles n = e, e + 2, ... through accumulator pair e.
     // Abort-safe: a failed wait marks the warp dead; it keeps walking its tiles
@@ -273,10 +281,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int ti = row / G, hl = row % G;
     const float sl2 = a.scale * kLog2e;
     bool dead = false;
+    // the row's list entry (token, slot) is read one tile ahead: its global
+    // load then overlaps the wait for the scores instead of stalling the O store
+    int t_nx = a.T, slot_nx = 0;
+    bool valid_nx = e < ntiles && tile_token(e, ti, t_nx, slot_nx);
     for (int n = e; n < ntiles; n += 2) {
       const int b = e, ph = (n >> 1) & 1;
-      int t, slot;
-      const bool valid = tile_token(n, ti, t, slot);
+      const int t = t_nx, slot = slot_nx;
+      const bool valid = valid_nx;
+      if (n + 2 < ntiles) valid_nx = tile_token(n + 2, ti, t_nx, slot_nx);
       const bool diag = n < ndiag;
       const int qpos = n * TPT + ti;  // position inside the block (diagonal tiles)
       dead = dead || !wait_bar_warp(bar(b_sfull(b)), ph, abort_flag, a.status,
@@ -403,8 +416,15 @@ template <int D, int G>
 cudaError_t launch_fwd_t(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st) {
   const size_t smem = 1024 + (2 + kFwdQStages) * (128 * D * 2) + 8 * kFwdStageWarp + 256;
-  cudaError_t e = cudaFuncSetAttribute(k_fwd<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  // The warpgroups' register budgets are drawn from the registers the block
+  // is launched with; a larger sum would leave setmaxnreg.inc waiting.
+  constexpr int kBudget = 2 * 128 * kFwdRegsSoftmax + 128 * kFwdRegsCtl;
+  static_assert(kBudget <= 65536, "register budgets exceed the register file");
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, k_fwd<D, G>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * kFwdThreads < kBudget) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(k_fwd<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   k_fwd<D, G><<<s.nb_bound * s.hkv, kFwdThreads, smem, st>>>(mq, mk, mv, a);
   return cudaGetLastError();
