@@ -636,20 +636,25 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+E2E_DEPTH = 3
+
+
 def run_e2e(w, inp, step, fl, K, W, world) -> dict:
     """The same metric end to end through the library's host-input API
     (HostInputStep): every step copies its inputs from pinned host memory to
     the device and its results (O, LSE, the five gradients and the loss) back
     to pinned host memory, all inside the timed region.  The copies run on two
     copy streams and overlap the kernels (inputs of later calls and of the next
-    step; O during the backward; the gradients during the next step's
-    selection and forward)."""
+    steps; O during the backward; the gradients during the next steps).  Three
+    input and output sets rotate (E2E_DEPTH), so a copy that runs slow for a
+    while (host-link copy rates vary from step to step) holds the kernels back
+    only once it is two steps behind."""
     from block_sparse_attention_proxy_gb300.step import HostInputStep
 
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     names_in = ("q", "k", "v", "q_p", "k_p", "dO", "cu_seqlens")
     host_in = {n: inp[n].to("cpu").pin_memory() for n in names_in}
-    hs = HostInputStep(step.params, inp, step=step)
+    hs = HostInputStep(step.params, inp, step=step, depth=E2E_DEPTH)
     host_out = hs.allocate_host_outputs()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
@@ -692,7 +697,7 @@ def run_e2e(w, inp, step, fl, K, W, world) -> dict:
     return dict(value=round(fl * world / ms_e2e / 1e9, 3), unit=UNIT,
                 ms_per_step=round(ms_e2e, 3), h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
                 tokens_per_s=round(w.total_tokens * world / ms_e2e * 1e3, 1),
-                returned=list(host_out),
+                returned=list(host_out), buffer_sets=E2E_DEPTH,
                 h2d_gb_per_s_alone=round(h2d / (c0.elapsed_time(c1) * 1e6), 1),
                 d2h_gb_per_s_alone=round(d2h / (c2.elapsed_time(c3) * 1e6), 1))
 

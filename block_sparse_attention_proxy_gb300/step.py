@@ -75,39 +75,48 @@ class HostInputStep:
     The host-to-device copies run on a copy stream in the order the calls need
     them (cu_seqlens, q_p, k_p for the selection; k, v, q for the forward; dO
     for the backward), and each call waits only for its own inputs, so the
-    copies of the later inputs overlap the earlier kernels.  Two sets of device
-    input buffers alternate between steps: the copies of step i also overlap
-    the kernels of step i-1, and wait only for step i-2's kernels, the last to
-    read the set they overwrite.
+    copies of the later inputs overlap the earlier kernels.  `depth` sets of
+    device input buffers and of device outputs rotate between steps: the
+    copies of step i overlap the kernels of the steps before it and wait only
+    for step i - depth's kernels, the last to read the input set they
+    overwrite.
 
     Results go back on a second copy stream: O (and LSE) as soon as the
     forward has finished, so their copy overlaps the backward; the five
     gradients and the proxy-KL loss after the backward, overlapping the next
-    step's selection and forward.  The next step's forward and backward wait
-    for those copies before overwriting the device outputs.  Without
-    `host_out`, only the loss is copied back (to `self.loss`).  Read host
-    results after synchronising.  The host tensors are read and written
-    asynchronously: leave the inputs unchanged, and do not read the outputs,
-    until the step's copies have finished.
+    steps.  A step's forward and backward wait only for the copies out of the
+    output set they overwrite, made depth steps earlier, so a copy that runs
+    slow for a while (host-link copy rates vary) holds the kernels back only
+    once it is more than depth - 1 steps behind.  Without `host_out`, only the loss is
+    copied back (to `self.loss`).  Read host results after synchronising.
+    The host tensors are read and written asynchronously: leave the inputs
+    unchanged, and do not read the outputs, until the step's copies have
+    finished.
     """
 
     GROUPS = (("cu_seqlens", "q_p", "k_p"), ("k", "v", "q"), ("dO",))
     FWD_OUT = ("o", "lse")
     BWD_OUT = ("dq", "dk", "dv", "dq_p", "dk_p", "kl_loss")
 
-    def __init__(self, params, like: dict, device="cuda", step: MSAStep | None = None):
+    def __init__(self, params, like: dict, device="cuda", step: MSAStep | None = None,
+                 depth: int = 2):
         """like: tensors with the shapes and dtypes of one step's inputs; step:
-        an MSAStep of these params whose outputs and workspace to use."""
+        an MSAStep of these params whose workspace (and first output set) to
+        use; depth: input and output sets in rotation (at least 1)."""
+        if depth < 1:
+            raise ValueError("HostInputStep: depth must be at least 1")
         self.step = step if step is not None else MSAStep(params, device)
+        self.depth = depth
         names = [n for grp in self.GROUPS for n in grp]
         self.bufs = [{n: torch.empty(like[n].shape, dtype=like[n].dtype, device=device)
-                      for n in names} for _ in range(2)]
-        self.done = [None, None]  # kernels of the last step that read buffer set b
+                      for n in names} for _ in range(depth)]
+        self.outs = [self.step.out] + [allocate_outputs(params, device) for _ in range(depth - 1)]
+        self.done = [None] * depth  # kernels of the last step that read input set b
+        self.fwd_copied = [None] * depth  # copies of O / gradients out of output set b
+        self.bwd_copied = [None] * depth
         self.copy_stream = torch.cuda.Stream(device)
         self.out_stream = torch.cuda.Stream(device)
         self.loss = torch.empty(1, dtype=torch.float64).pin_memory()
-        self._fwd_out_copied = None  # copies of the previous step's O / gradients
-        self._bwd_out_copied = None
         self._n = 0
 
     def allocate_host_outputs(self) -> dict:
@@ -119,7 +128,8 @@ class HostInputStep:
     def __call__(self, host_inp: dict, loss_out: torch.Tensor | None = None,
                  host_out: dict | None = None) -> dict:
         """Queue one step on the current stream; returns the device outputs
-        (valid until the next step's kernels overwrite them)."""
+        (valid until the kernels of the step depth calls later overwrite
+        them)."""
         for grp in self.GROUPS:
             for n in grp:
                 t = host_inp[n]
@@ -131,7 +141,7 @@ class HostInputStep:
                 t = host_out[n]
                 if t.is_cuda or not t.is_pinned():
                     raise ValueError(f"HostInputStep: output {n!r} must be a pinned host tensor")
-        b = self._n & 1
+        b = self._n % self.depth
         self._n += 1
         dev, cs, os_ = self.bufs[b], self.copy_stream, self.out_stream
         st = torch.cuda.current_stream(cs.device)
@@ -145,12 +155,13 @@ class HostInputStep:
                 ev = torch.cuda.Event()
                 ev.record(cs)
                 ready.append(ev)
-        out = self.step.out
+        out = self.outs[b]
+        self.step.out = out
         st.wait_event(ready[0])
         self.step.select(dev, st)
         st.wait_event(ready[1])
-        if self._fwd_out_copied is not None:  # the previous step's O has left
-            st.wait_event(self._fwd_out_copied)
+        if self.fwd_copied[b] is not None:  # this set's O of depth steps ago has left
+            st.wait_event(self.fwd_copied[b])
         self.step.forward(dev, st)
         if host_out is not None:
             fwd_done = torch.cuda.Event()
@@ -159,11 +170,11 @@ class HostInputStep:
             with torch.cuda.stream(os_):
                 for n in self.FWD_OUT:
                     host_out[n].copy_(out[n], non_blocking=True)
-            self._fwd_out_copied = torch.cuda.Event()
-            self._fwd_out_copied.record(os_)
+            self.fwd_copied[b] = torch.cuda.Event()
+            self.fwd_copied[b].record(os_)
         st.wait_event(ready[2])
-        if self._bwd_out_copied is not None:  # the previous step's gradients have left
-            st.wait_event(self._bwd_out_copied)
+        if self.bwd_copied[b] is not None:  # this set's gradients of depth steps ago have left
+            st.wait_event(self.bwd_copied[b])
         self.step.backward(dev, st)
         done = torch.cuda.Event()
         done.record(st)
@@ -175,15 +186,15 @@ class HostInputStep:
             with torch.cuda.stream(os_):
                 for n in self.BWD_OUT:
                     host_out[n].copy_(out[n], non_blocking=True)
-            self._bwd_out_copied = torch.cuda.Event()
-            self._bwd_out_copied.record(os_)
+            self.bwd_copied[b] = torch.cuda.Event()
+            self.bwd_copied[b].record(os_)
         return out
 
     def wait_outputs(self, stream=None) -> None:
         """Makes `stream` (default: the current one) wait for the result copies
         queued so far."""
         st = stream if stream is not None else torch.cuda.current_stream(self.out_stream.device)
-        for ev in (self._fwd_out_copied, self._bwd_out_copied):
+        for ev in self.fwd_copied + self.bwd_copied:
             if ev is not None:
                 st.wait_event(ev)
 

@@ -1,6 +1,6 @@
 """HostInputStep: inputs in pinned host memory, copied on a copy stream that
-overlaps the kernels (within a step, and across steps through two alternating
-device buffer sets).  Steps queued back to back, with no synchronisation in
+overlaps the kernels (within a step, and across steps through rotating device
+buffer and output sets).  Steps queued back to back, with no synchronisation in
 between, must return bit for bit what MSAStep returns on device inputs; the
 fourth step reuses the first buffer set, so a copy that overtook the kernels
 still reading that set would show."""
@@ -55,11 +55,13 @@ def test_host_input_step_rejects_pageable_inputs():
         hs(inp)  # pageable CPU tensors
 
 
-def test_host_outputs_of_every_step_match_device_steps():
+@pytest.mark.parametrize("depth", [1, 2, 3])
+def test_host_outputs_of_every_step_match_device_steps(depth):
     """With host_out, O, LSE, the five gradients and the loss of every step
     come back to pinned host memory while later steps run; each step's copy
     must hold that step's results bit for bit (a copy that a later step's
-    kernels overtook would hold the later step's values)."""
+    kernels overtook would hold the later step's values).  depth input and
+    output sets rotate; five steps wrap around each of them."""
     from block_sparse_attention_proxy_gb300 import msa_get_device_status
     from block_sparse_attention_proxy_gb300.step import HostInputStep, MSAStep, params_for
 
@@ -74,7 +76,7 @@ def test_host_outputs_of_every_step_match_device_steps():
         torch.cuda.synchronize()
         ref.append({n: v.cpu() for n, v in out.items()})
     host = [{n: v.pin_memory() for n, v in inp.items()} for inp in sets]
-    hs = HostInputStep(prm, sets[0])
+    hs = HostInputStep(prm, sets[0], depth=depth)
     order = [0, 1, 2, 0, 1]
     outs = [hs.allocate_host_outputs() for _ in order]
     for j, i in enumerate(order):
