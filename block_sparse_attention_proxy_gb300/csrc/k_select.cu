@@ -43,6 +43,10 @@ constexpr int kSelEpiGroups = 3;
 constexpr int kSelProducerWarp = 12, kSelMmaWarp = 13;
 constexpr uint32_t kSelRegsEpi = 152, kSelRegsCtl = 56;
 constexpr float kTieBand = 1e-3f;
+// CTAs per cluster: query blocks gb0, gb0 - 1, ... of one group, which share
+// their key blocks' k_p rows by multicast (2 or 4).  Four measured slower at
+// 128k-1M: at most 36 clusters of four are resident, 144 of the 152 SMs.
+constexpr int kSelCluster = 2;
 
 // k_p ring stages (two key blocks each).  The TMA latency of a stage is about
 // 3000 SM cycles at 128k, three steps' worth; six stages measured no faster.
@@ -170,21 +174,25 @@ __global__ void __launch_bounds__(kSelThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item.  A cluster of two CTAs takes query blocks gb0 and gb0 - 1
-  // of group g (heaviest first); CTA `rank` takes gb0 - rank.  When both lie
-  // in one document (paired), their key blocks 0..J-1 are the same k_p rows:
-  // each CTA loads one of the two key blocks of a step and multicasts it to
-  // both, so the pair reads k_p from L2 once instead of twice. ----
+  // ---- work item.  A cluster of kSelCluster CTAs takes query blocks gb0,
+  // gb0 - 1, ... of group g (heaviest first); CTA `rank` takes gb0 - rank.
+  // When all of them lie in one document (shared), their first key blocks
+  // are the same k_p rows: each of a step's two key blocks is loaded by one
+  // CTA and multicast to all, so the cluster reads k_p from L2 once instead
+  // of kSelCluster times.  With two CTAs, rank r loads block 2m + r of step
+  // m; with four, ranks 0-1 load the blocks of even steps, ranks 2-3 those
+  // of odd steps. ----
   const uint32_t rank = cluster_ctarank();
   const bool ok_batch = a.cu_blocks[a.ndoc + 1] != 0;  // else malformed cu_seqlens (flagged by k_meta)
   const int nbt = min(a.cu_blocks[a.ndoc], a.nb_bound);
-  const int cl = (int)(blockIdx.x >> 1);
+  const int cl = (int)(blockIdx.x / kSelCluster);
   const int g = cl % a.hkv;
-  const int gb0 = nbt - 1 - 2 * (cl / a.hkv);
+  const int gb0 = nbt - 1 - kSelCluster * (cl / a.hkv);
   const int gb = gb0 - (int)rank;
   const bool has = ok_batch && gb >= 0;  // warp- and CTA-uniform
-  const bool paired = ok_batch && gb0 >= 1 &&
-                      doc_of_block(a.cu_blocks, a.ndoc, gb0) == doc_of_block(a.cu_blocks, a.ndoc, gb0 - 1);
+  const bool shared_kp = ok_batch && gb0 >= kSelCluster - 1 &&
+                      doc_of_block(a.cu_blocks, a.ndoc, gb0) ==
+                          doc_of_block(a.cu_blocks, a.ndoc, gb0 - (kSelCluster - 1));
   const int d = has ? doc_of_block(a.cu_blocks, a.ndoc, gb) : 0;
   const int J = has ? gb - a.cu_blocks[d] : 0;
   const int dstart = has ? a.cu[d] : 0;
@@ -193,16 +201,17 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   const int nrows = min(kBlock, L - J * kBlock);
   const int nblk = has ? J + 1 : 0;
   const int nstep = (nblk + 1) / 2;  // steps of two key blocks (the last may hold one)
-  // Steps both CTAs of a pair take (rank 1's count; rank 0 may have one more,
-  // which it loads alone); 0 when not paired.
-  const int common = paired ? (J - (int)(rank == 0) + 2) / 2 : 0;
-  constexpr uint16_t kPair = 0x3;
+  // Steps every CTA of the cluster takes (the last rank's count, with J0 =
+  // J + rank the first rank's block; lower ranks load their one or two extra
+  // steps alone); 0 when not shared.
+  const int common = shared_kp ? (J + (int)rank - (kSelCluster - 1) + 2) / 2 : 0;
+  constexpr uint16_t kMcMask = (uint16_t)((1u << kSelCluster) - 1);
 
   if (threadIdx.x == 0) {
     mbar_init(b_qfull, 1);
     for (int s = 0; s < kSelStages; ++s) {
       mbar_init(b_kvfull(s), 1);
-      mbar_init(b_kvempty(s), paired ? 2 : 1);  // a paired stage is released by both MMA warps
+      mbar_init(b_kvempty(s), shared_kp ? kSelCluster : 1);  // a shared stage: every CTA's MMA warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_accfull(i), 1);
@@ -248,9 +257,11 @@ __global__ void __launch_bounds__(kSelThreads, 1)
             break;
           mbar_arrive_expect_tx(b_kvfull(s), 2 * C::kTileBytes);
           const uint32_t dst = smem_u32(sK + s * 2 * C::kTileBytes);
-          if (m < common) {  // this CTA's key block of the step, for both CTAs
-            tma_load_3d_mc(dst + rank * C::kTileBytes, &tm_kp, b_kvfull(s), 0, g,
-                           dstart + (2 * m + (int)rank) * kBlock, kPair);
+          if (m < common) {  // this CTA's key block of the step, if any, for every CTA
+            const int u = (int)(rank & 1);
+            if (kSelCluster == 2 || (int)(rank >> 1) == (m & 1))
+              tma_load_3d_mc(dst + u * C::kTileBytes, &tm_kp, b_kvfull(s), 0, g,
+                             dstart + (2 * m + u) * kBlock, kMcMask);
           } else {
             tma_load_3d(dst, &tm_kp, b_kvfull(s), 0, g, dstart + 2 * m * kBlock);
             tma_load_3d(dst + C::kTileBytes, &tm_kp, b_kvfull(s), 0, g,
@@ -287,7 +298,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
               const uint64_t bd = make_sdesc(k0 + kk * 32, 16, C::kSBO, C::kLayout);
               umma_bf16(tbase + acc * 256, ad, bd, idesc, kk > 0);
             }
-            if (m < common) umma_commit_mc(b_kvempty(s), kPair);  // both CTAs' copies of the stage
+            if (m < common) umma_commit_mc(b_kvempty(s), kMcMask);  // every CTA's copy of the stage
             else umma_commit(b_kvempty(s));
             umma_commit(b_accfull(acc));
           }
@@ -541,15 +552,16 @@ cudaError_t launch_sel_t(const Shape& s, const CUtensorMap& mq, const CUtensorMa
   e = cudaFuncSetAttribute(k_select<DP, CAP, ARG, WIN>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // clusters of two CTAs: query blocks gb0 and gb0 - 1 of one group
+  // clusters of kSelCluster CTAs: query blocks gb0, gb0 - 1, ... of one group
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(2 * s.hkv * ((s.nb_bound + 1) / 2)));
+  cfg.gridDim =
+      dim3((unsigned)(kSelCluster * s.hkv * ((s.nb_bound + kSelCluster - 1) / kSelCluster)));
   cfg.blockDim = dim3(kSelThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = kSelCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -581,7 +593,7 @@ cudaError_t launch_select(const Shape& s, const int32_t* cu_seqlens, const int32
   const int sw = s.dp == 64 ? 128 : 64;
   cudaError_t e;
   if ((e = make_tmap_3d(&mq, q_p, s.dp, s.hkv, s.T, s.dp, 1, 128, sw)) != cudaSuccess) return e;
-  // one 128-row key block per box (a step loads two, or one per CTA of a pair)
+  // one 128-row key block per box (a step loads two, or each loading CTA of a cluster one)
   if ((e = make_tmap_3d(&mk, k_p, s.dp, s.hkv, s.T, s.dp, 1, 128, sw)) != cudaSuccess) return e;
   SelArgs a{cu_seqlens, cu_blocks, s.ndoc,   s.T,         s.hkv, s.K,
             s.nb_bound, s.window,  s.dilation, s.proxy_scale, sel_idx, sel_score,
