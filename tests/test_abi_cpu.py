@@ -111,3 +111,14 @@ def test_launch_counter_starts_at_zero_without_gpu(m):
     if torch.cuda.is_available():
         pytest.skip("counter may have advanced in this process")
     assert m.msa_launch_count() == 0
+
+
+def test_host_input_step_needs_one_buffer_set(m):
+    """The host-input step rotates `depth` sets of device buffers; fewer than
+    one is rejected before any device memory is touched."""
+    from block_sparse_attention_proxy_gb300.step import HostInputStep
+
+    prm = m.make_params(1024, 1, 1024, 4, 1, 64, 32, 4)
+    for depth in (0, -1):
+        with pytest.raises(ValueError):
+            HostInputStep(prm, {}, device="cpu", depth=depth)
