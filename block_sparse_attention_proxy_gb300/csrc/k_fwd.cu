@@ -20,7 +20,7 @@
 // Roles (384 threads): two softmax warpgroups (warps 0-3 and 4-7) take
 // alternate tiles through two S/O accumulator pairs, so one warpgroup's
 // softmax overlaps the other's P V product and O stores; warp 8 is the TMA
-// producer (regroup entries read one tile ahead, three Q stages); warp 9 issues
+// producer (regroup entries read one tile ahead, four Q stages); warp 9 issues
 // the MMAs; warps 10-11 only complete the third warpgroup, so that register
 // budgets can be set per warpgroup (setmaxnreg): 2 x 128 x 200 for the softmax
 // warps, 128 x 104 for the producer and MMA warps, 64512 = 384 x 168 in all (at
@@ -34,11 +34,12 @@ namespace {
 
 constexpr int kFwdThreads = 384;
 constexpr uint32_t kFwdRegsSoftmax = 200, kFwdRegsCtl = 104;
-constexpr int kFwdQStages = 3;
+constexpr int kFwdQStages = 4;
 // Per softmax warp: a 32-row x 64-column int16 staging tile (128B-swizzled
-// rows) and the 32 row pointers, used to turn row-per-thread O values into
-// row-contiguous 128-byte segments, four rows per warp store.
-constexpr int kFwdStageWarp = 4096 + 256;
+// rows) and the 32 partial-row indices (-1: no row), used to turn
+// row-per-thread O values into row-contiguous 128-byte segments, four rows
+// per warp store.
+constexpr int kFwdStageWarp = 4096 + 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct FwdArgs {
@@ -361,9 +362,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float mo = __uint_as_float(mbits);
         const float qf = q16_factor(mo);
         uint8_t* stg = sOst + warp * kFwdStageWarp;
-        int16_t** rowp = reinterpret_cast<int16_t**>(stg + 4096);
+        // partial rows of one query chunk: < 262144 tokens x 255 heads x 16 slots < 2^31
+        int32_t* rowi = reinterpret_cast<int32_t*>(stg + 4096);
         const size_t prow = ((size_t)(t - t0) * a.hq + g * G + hl) * a.K + slot;
-        rowp[lane] = valid ? a.o_part + prow * (size_t)D : nullptr;
+        rowi[lane] = valid ? (int32_t)prow : -1;
 #pragma unroll 1
         for (int c = 0; c < D / 64; ++c) {
           uint32_t va[32], vb[32];
@@ -385,8 +387,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int i = 0; i < 8; ++i) {
             const int rr = (lane >> 3) + 4 * i;
             const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
-            int16_t* dst = rowp[rr];
-            if (dst != nullptr) *reinterpret_cast<uint4*>(dst + c * 64 + ch * 8) = x;
+            const int32_t ri = rowi[rr];
+            if (ri >= 0)
+              *reinterpret_cast<uint4*>(a.o_part + (size_t)ri * D + c * 64 + ch * 8) = x;
           }
           __syncwarp();
         }
@@ -416,6 +419,8 @@ template <int D, int G>
 cudaError_t launch_fwd_t(const Shape& s, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st) {
   const size_t smem = 1024 + (2 + kFwdQStages) * (128 * D * 2) + 8 * kFwdStageWarp + 256;
+  static_assert(1024 + (2 + kFwdQStages) * (128 * 128 * 2) + 8 * kFwdStageWarp + 256 <= 232448,
+                "shared memory budget");
   // The warpgroups' register budgets are drawn from the registers the block
   // is launched with; a larger sum would leave setmaxnreg.inc waiting.
   constexpr int kBudget = 2 * 128 * kFwdRegsSoftmax + 128 * kFwdRegsCtl;
